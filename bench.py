@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Decode throughput of the QSA sparse path on GB300: rows/s of one decode
+step (qsa_select_paged_tokens + qsa_sparse_attention) and the achieved HBM
+bandwidth of the selection stage against the measured copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 4]
+
+Workload (default): 256 rows x 131072 tokens -- 32768 compressed keys per row
+(256 compressed pages), 256 K/V pages of 512 tokens per row, pages randomly
+permuted, FP16, about 34 GB resident per GPU; every step streams ~2.7 GB, far
+more than the 129 MB L2, so no L2 flush is needed between steps.
+
+Timing: W warm-up steps, then K steps bracketed by a barrier and a device
+synchronize, timed with CUDA events on the launching stream; max over ranks.
+N > 1 (torchrun): every rank runs its own 256 rows (weak scaling, no
+collective on the data path); value = all ranks' rows / max time.
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on the
+host cores on a bounded sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode rows/s (select+sparse attend) and achieved HBM GB/s vs GB300 peak"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --- algorithmic bytes (what the method must move; duplicates once) ----------
+
+def select_bytes_per_row(seq_len: int, pos: int) -> int:
+    """visible keys (256 B each) + q_sel + page-table entries + index write +
+    row metadata (request id, seq_len, position)."""
+    V = max(0, min((pos + 1) // 4, seq_len // 4))
+    return 256 * V + 4 * 128 * 2 + 4 * math.ceil(V / 128) + 4 * 2051 + 4 + 4 + 8
+
+
+def attend_bytes_per_row(idx_row: np.ndarray) -> int:
+    """distinct valid tokens (1 KiB K+V each) + q + out + index read + the
+    K/V page-table entries touched + request id."""
+    v = np.unique(idx_row[idx_row >= 0])
+    pages = np.unique(v // 512).size
+    return 1024 * v.size + 3 * 256 * 2 * 2 + 4 * idx_row.size + 4 * pages + 4
+
+
+# --- clocks during the timed region ----------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# --- distributed plumbing (host-side only) -----------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# --- CPU oracle baseline -----------------------------------------------------
+
+class OracleSample:
+    """Host copies of a few rows of a workload (their queries, tables and the
+    pages they reference) so the CPU oracle can run one decode row at a time."""
+
+    def __init__(self, w, rows):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.rows = list(rows)
+        t2r = w.token_to_request.cpu().numpy()
+        self.cpt = w.cmp_page_table.cpu().numpy()
+        self.kpt = w.kv_page_table.cpu().numpy()
+        reqs = sorted({int(t2r[r]) for r in self.rows})
+        self.q = w.q_sel.cpu().numpy()
+        self.qa = w.q_attn.cpu().numpy()
+        self.t2r, self.sl = t2r, w.seq_lens.cpu().numpy()
+        self.qp = w.query_positions.cpu().numpy()
+        self.cpool = self._pool(w.cmp_cache, self.cpt[reqs].ravel(), 128 * 128)
+        self.kpool = self._pool(w.kv_cache, self.kpt[reqs].ravel(), 512 * 512)
+
+    def _pool(self, cache, ids, halves):
+        P = cache.shape[0]
+        ids = sorted({int(p) for p in ids if 0 <= int(p) < P})
+        sel = torch.tensor(ids, dtype=torch.long, device=cache.device)
+        host = cache.index_select(0, sel).cpu().numpy().reshape(len(ids), -1)
+        return self.oracle.PagePool({p: host[i] for i, p in enumerate(ids)}, num_pages=P,
+                                    page_halves=halves)
+
+    def run_row(self, k: int):
+        """One decode row on the oracle: selection, then attention on it."""
+        r = self.rows[k % len(self.rows)]
+        o = self.oracle
+        idx, _ = o.select(self.q[r:r + 1], self.cpool, self.cpt, self.t2r[r:r + 1], self.sl,
+                          self.qp[r:r + 1])
+        o.attention(self.qa[r:r + 1], self.kpool, self.kpt, self.t2r[r:r + 1], idx)
+
+
+def oracle_rate(sample: OracleSample, n_rows: int, threads: int):
+    """Rows/s of the oracle over n_rows decode rows spread over `threads` OS
+    threads (the C code releases the GIL); returns (rows/s, wall seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(sample.run_row, range(n_rows)))
+    dt = time.perf_counter() - t0
+    return n_rows / dt, dt
+
+
+def _sample_workload(workload: int, rows: int, rank: int):
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    if torch.cuda.is_available():
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        w = W.config(workload, device=dev, seed=1000 + workload + 7919 * rank)
+    else:
+        w = W.config(workload, device="cpu", rows=rows, seed=1000 + workload + 7919 * rank)
+    return w
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores.  One
+    step = one decode row of the workload (select + attend); the K timed steps
+    run spread over the host threads."""
+    if rank != 0:
+        return 0
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    threads = max(1, min(os.cpu_count() or 1, 16))
+    w = _sample_workload(args.workload, threads, rank)
+    sample = OracleSample(w, range(min(threads, w.R)))
+    del w
+    oracle_rate(sample, min(args.warmup, threads), threads)      # warm-up rows
+    value, dt = oracle_rate(sample, args.steps, threads)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
+        "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[args.workload], "rows_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} decode rows (select+attend) cycling over "
+                                   f"{len(sample.rows)} rows of {W.CONFIG_NAMES[args.workload]}, "
+                                   f"plain C oracle on {threads} threads, {dt:.1f} s wall"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --- our arm -----------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import sparse_paged_attention_qsa_gb300 as qsa
+    from sparse_paged_attention_qsa_gb300 import build as qbuild
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the product path has no CPU fallback)")
+    qbuild.build()
+    qsa.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+
+    w = W.config(args.workload, device=dev, seed=1000 + args.workload + 7919 * rank,
+                 rows=args.rows)
+    R = w.R
+    stream = torch.cuda.current_stream(dev)
+    idx = torch.empty((R, 2051), dtype=torch.int32, device=dev)
+    out = torch.empty((R, 3, 256), dtype=torch.float16, device=dev)
+    sel_ws = torch.empty(qsa.qsa_select_workspace_bytes(R, w.cmp_page_table.shape[1]),
+                         dtype=torch.uint8, device=dev)
+    att_ws = torch.empty(qsa.qsa_attention_workspace_bytes(R, 2051), dtype=torch.uint8,
+                         device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    k_view, v_view = w.k_view, w.v_view
+
+    def select():
+        qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                                    w.seq_lens, w.query_positions, out=idx, workspace=sel_ws,
+                                    error_word=err, stream=stream)
+
+    def attend():
+        qsa.qsa_sparse_attention(w.q_attn, k_view, v_view, w.kv_page_table, w.token_to_request,
+                                 idx, out=out, workspace=att_ws, error_word=err, stream=stream)
+
+    for _ in range(args.warmup):
+        select()
+        attend()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise SystemExit(f"bench.py: device error word {int(err.item())}")
+
+    # algorithmic bytes of this workload (from the produced index lists)
+    seq = w.seq_lens.cpu().numpy()
+    pos = w.query_positions.cpu().numpy()
+    t2r = w.token_to_request.cpu().numpy()
+    idx_h = idx.cpu().numpy()
+    sel_bytes = sum(select_bytes_per_row(int(seq[t2r[r]]), int(pos[r])) for r in range(R))
+    att_bytes = sum(attend_bytes_per_row(idx_h[r]) for r in range(R))
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            select()
+            ev[i][1].record(stream)
+            attend()
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    t_step = max_over_ranks(total_ms / K, world, dev)
+    value = R * world / (t_step * 1e-3)
+
+    # end to end through the public API: per-step inputs from pinned host
+    # memory, results read back to pinned host memory, inside the timed region
+    h_in = {n: getattr(w, n).cpu().pin_memory() for n in
+            ("q_sel", "q_attn", "token_to_request", "seq_lens", "query_positions",
+             "cmp_page_table", "kv_page_table")}
+    h_idx = torch.empty((R, 2051), dtype=torch.int32).pin_memory()
+    h_out = torch.empty((R, 3, 256), dtype=torch.float16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_idx.numel() * 4 + h_out.numel() * 2
+    Ke = max(1, min(K, args.e2e_steps))
+
+    def e2e_step():
+        for n, t in h_in.items():
+            getattr(w, n).copy_(t, non_blocking=True)
+        qsa.qsa_decode(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request, w.seq_lens,
+                       w.query_positions, w.q_attn, k_view, v_view, w.kv_page_table,
+                       indices=idx, out=out, sel_workspace=sel_ws, att_workspace=att_ws,
+                       error_word=err, stream=stream)
+        h_idx.copy_(idx, non_blocking=True)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_step_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, dev)
+    e2e_value = R * world / (e2e_step_ms * 1e-3)
+    if int(err.item()) != 0:
+        raise SystemExit(f"bench.py: device error word {int(err.item())}")
+
+    peak, peak_kind = _peaks()
+    sel_gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
+    att_gbs = att_bytes / (att_ms * 1e-3) / 1e9
+    step_gbs = (sel_bytes + att_bytes) / (total_ms / K * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = max(1, min(os.cpu_count() or 1, 16))
+        sample = OracleSample(w, range(min(threads, R)))
+        n = 2 * len(sample.rows)
+        rate, dt = oracle_rate(sample, n, threads)
+        cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} decode rows (select+attend) over {len(sample.rows)} rows of "
+                         f"this workload, plain C oracle on {threads} threads, {dt:.1f} s wall"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[args.workload], "rows_per_gpu": R,
+                   "seq_len": int(seq[0]), "storage_dtype": "f16",
+                   "l2": "inputs larger than L2 (each step streams "
+                         f"{(sel_bytes + att_bytes) / 1e9:.2f} GB of a "
+                         f"{(w.cmp_cache.numel() + w.kv_cache.numel()) * 2 / 1e9:.1f} GB "
+                         "resident set; no flush)",
+                   "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+                   "select_ms": sel_ms, "attend_ms": att_ms, "attend_hbm_gbs": att_gbs,
+                   "algorithmic_bytes_per_step": sel_bytes + att_bytes,
+                   "parallelism": f"rows sharded over {world} GPU(s), no collective"},
+        "roofline": {"bound": "hbm", "kernel": "selection stage (score + top-k launches)",
+                     "achieved": sel_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": sel_gbs / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": sel_bytes, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms, "steps": Ke},
+        "gpu_launches": 4 * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--rows", type=int, default=None,
+                    help="keep only the first rows of a multi-row workload (profiling cases)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("bench.py: at least 3 warm-up steps are required")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

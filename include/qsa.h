@@ -42,6 +42,12 @@
 extern "C" {
 #endif
 
+#if defined(__GNUC__)
+#define QSA_API __attribute__((visibility("default")))
+#else
+#define QSA_API
+#endif
+
 /* Fixed contract ("Exact contracts" / Selection and Attention). */
 #define QSA_TOKEN_TOPK       2048  /* tokens selected from compressed blocks */
 #define QSA_COMPRESS_RATIO   4     /* tokens per compressed key */
@@ -87,17 +93,17 @@ typedef int qsa_dtype;
 typedef struct CUstream_st* qsa_stream_t;  /* == cudaStream_t; NULL = legacy */
 
 /* Human-readable name of a status code (static storage). */
-const char* qsa_status_string(qsa_status status);
+QSA_API const char* qsa_status_string(qsa_status status);
 
 /* Library version: major*10000 + minor*100 + patch. */
-int qsa_version(void);
+QSA_API int qsa_version(void);
 
 /*
  * Workspace for qsa_select_paged_tokens: bytes needed for num_rows rows whose
  * compressed page table has cmp_pt_cols columns (each row may hold up to
  * cmp_pt_cols*128 visible blocks).  Alignment 256 bytes.
  */
-size_t qsa_select_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols);
+QSA_API size_t qsa_select_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols);
 
 /*
  * qsa_select_paged_tokens -- per row r:
@@ -131,7 +137,7 @@ size_t qsa_select_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols);
  *   error_word       device uint32 or NULL (QSA_DERR_* bits ORed in)
  *   stream           launch stream
  */
-qsa_status qsa_select_paged_tokens(
+QSA_API qsa_status qsa_select_paged_tokens(
     const void* q_sel, qsa_dtype q_sel_dtype, int64_t num_rows,
     const int64_t q_sel_strides[3],
     const void* cmp_cache, qsa_dtype cmp_dtype, const int64_t cmp_shape[4],
@@ -150,7 +156,7 @@ qsa_status qsa_select_paged_tokens(
  * Workspace for qsa_sparse_attention: bytes needed for num_rows rows of
  * index_width logical indices.  Alignment 256 bytes.
  */
-size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width);
+QSA_API size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width);
 
 /*
  * qsa_sparse_attention -- per row r and head h < 3:
@@ -177,7 +183,7 @@ size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width);
  *   workspace        >= qsa_attention_workspace_bytes(num_rows, index_width)
  *   error_word       device uint32 or NULL
  */
-qsa_status qsa_sparse_attention(
+QSA_API qsa_status qsa_sparse_attention(
     const void* q, qsa_dtype q_dtype, int64_t num_rows, const int64_t q_strides[3],
     const void* k_cache, const void* v_cache, qsa_dtype kv_dtype,
     const int64_t kv_shape[4], const int64_t k_strides[4], const int64_t v_strides[4],

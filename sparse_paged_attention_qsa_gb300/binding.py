@@ -1,0 +1,221 @@
+"""Thin ctypes binding over libqsa (include/qsa.h).
+
+Argument marshalling only: tensors become (data pointer, dtype tag, shape,
+strides); the stream is torch's current CUDA stream unless given.  Every step
+of the computation runs in libqsa's CUDA kernels.  PyTorch is used here for
+device memory (outputs and workspaces the caller did not pass) and streams.
+
+If libqsa.so has not been built the first call raises -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqsa.so")
+
+TOKEN_TOPK = 2048
+COMPRESS_RATIO = 4
+TOPK_BLOCKS = 512
+OUT_WIDTH = 2051
+DERR_REQUEST, DERR_CMP_PAGE, DERR_KV_PAGE = 1, 2, 4
+
+DT_F16, DT_BF16, DT_F32, DT_I32, DT_I64 = 1, 2, 3, 4, 5
+_DTYPE_TAG = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_F32,
+              torch.int32: DT_I32, torch.int64: DT_I64}
+
+STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE",
+          4: "QSA_ERR_STRIDE", 5: "QSA_ERR_ALIGN", 6: "QSA_ERR_CONTRACT",
+          7: "QSA_ERR_WORKSPACE", 8: "QSA_ERR_ALIAS", 9: "QSA_ERR_CUDA"}
+
+EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
+            "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
+            "qsa_sparse_attention")
+
+
+class QSAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libqsa.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libqsa.so not found at {path}; build it with "
+                "`python -m sparse_paged_attention_qsa_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        i32, i64, u64, vp, sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                 ctypes.c_void_p, ctypes.c_size_t)
+        p64 = ctypes.POINTER(ctypes.c_int64)
+        lib.qsa_status_string.restype = ctypes.c_char_p
+        lib.qsa_status_string.argtypes = [ctypes.c_int]
+        lib.qsa_version.restype = ctypes.c_int
+        lib.qsa_version.argtypes = []
+        lib.qsa_select_workspace_bytes.restype = sz
+        lib.qsa_select_workspace_bytes.argtypes = [i64, i64]
+        lib.qsa_attention_workspace_bytes.restype = sz
+        lib.qsa_attention_workspace_bytes.argtypes = [i64, i64]
+        lib.qsa_select_paged_tokens.restype = ctypes.c_int
+        lib.qsa_select_paged_tokens.argtypes = [
+            vp, ctypes.c_int, i64, p64,
+            vp, ctypes.c_int, p64, p64,
+            vp, ctypes.c_int, i64, i64, i64,
+            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+            i32, i32,
+            vp, ctypes.c_int, i64, i64,
+            vp, sz, vp, vp]
+        lib.qsa_sparse_attention.restype = ctypes.c_int
+        lib.qsa_sparse_attention.argtypes = [
+            vp, ctypes.c_int, i64, p64,
+            vp, vp, ctypes.c_int, p64, p64, p64,
+            vp, ctypes.c_int, i64, i64, i64,
+            vp, ctypes.c_int,
+            vp, ctypes.c_int, i64, i64,
+            ctypes.c_float,
+            vp, ctypes.c_int, p64,
+            vp, sz, vp, vp]
+        _lib = lib
+        return lib
+
+
+def _arr(vals):
+    vals = list(vals)
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
+def _tag(t: torch.Tensor) -> int:
+    return _DTYPE_TAG.get(t.dtype, 0)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else (t.data_ptr() or None)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int):
+    if status != 0:
+        raise QSAError(status, load_library().qsa_status_string(status).decode())
+
+
+def qsa_select_workspace_bytes(num_rows: int, cmp_pt_cols: int) -> int:
+    return int(load_library().qsa_select_workspace_bytes(num_rows, cmp_pt_cols))
+
+
+def qsa_attention_workspace_bytes(num_rows: int, index_width: int) -> int:
+    return int(load_library().qsa_attention_workspace_bytes(num_rows, index_width))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's CUDA allocator returns 512-byte aligned blocks
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def qsa_select_paged_tokens(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
+                            query_positions, token_topk: int = TOKEN_TOPK,
+                            compress_ratio: int = COMPRESS_RATIO, out=None, workspace=None,
+                            error_word=None, stream=None):
+    """Selection: returns out [R,2051] int32 (see include/qsa.h)."""
+    lib = load_library()
+    R = q_sel.shape[0] if q_sel.dim() == 3 else -1
+    if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
+        raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
+    if tuple(q_sel.shape[1:]) != (4, 128):
+        raise QSAError(3, "q_sel must be [R,4,128]")
+    if out is None:
+        out = torch.empty((R, OUT_WIDTH), dtype=torch.int32, device=q_sel.device)
+    if cmp_page_table.stride(1) != 1 and cmp_page_table.shape[1] > 1:
+        raise QSAError(4, "page table columns must be contiguous")
+    if out.dim() != 2 or (out.stride(1) != 1 and out.shape[1] > 1):
+        raise QSAError(4, "out must be [R,2051] with contiguous columns")
+    cols = cmp_page_table.shape[1]
+    need = qsa_select_workspace_bytes(R, cols)
+    if workspace is None:
+        workspace = _workspace(need, q_sel.device)
+    st = lib.qsa_select_paged_tokens(
+        _ptr(q_sel), _tag(q_sel), R, _arr(q_sel.stride()),
+        _ptr(cmp_cache), _tag(cmp_cache), _arr(cmp_cache.shape), _arr(cmp_cache.stride()),
+        _ptr(cmp_page_table), _tag(cmp_page_table), cmp_page_table.shape[0], cols,
+        cmp_page_table.stride(0),
+        _ptr(token_to_request), _tag(token_to_request), _ptr(seq_lens), _tag(seq_lens),
+        _ptr(query_positions), _tag(query_positions),
+        int(token_topk), int(compress_ratio),
+        _ptr(out), _tag(out), out.shape[1], out.stride(0),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(error_word), _stream(stream))
+    _check(st)
+    return out
+
+
+def qsa_sparse_attention(q, k_cache, v_cache, kv_page_table, token_to_request, indices,
+                         scale: float = 1.0 / 16.0, out=None, workspace=None, error_word=None,
+                         stream=None):
+    """Sparse attention: returns out [R,3,256] FP16 (see include/qsa.h).
+    k_cache / v_cache are the exact-packed views (strides [262144,512,256,1],
+    V at storage offset 256 of the same buffer)."""
+    lib = load_library()
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or indices.dim() != 2:
+        raise QSAError(3, "q [R,3,256], k/v [P,512,1,256], indices [R,W] expected")
+    if k_cache.shape != v_cache.shape:
+        raise QSAError(3, "k_cache and v_cache shapes differ")
+    R = q.shape[0]
+    if out is None:
+        out = torch.empty((R, 3, 256), dtype=torch.float16, device=q.device)
+    if kv_page_table.dim() != 2 or (kv_page_table.stride(1) != 1 and kv_page_table.shape[1] > 1):
+        raise QSAError(4, "page table must be 2-D with contiguous columns")
+    if indices.stride(1) != 1 and indices.shape[1] > 1:
+        raise QSAError(4, "index columns must be contiguous")
+    width = indices.shape[1]
+    need = qsa_attention_workspace_bytes(R, width)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    st = lib.qsa_sparse_attention(
+        _ptr(q), _tag(q), R, _arr(q.stride()),
+        _ptr(k_cache), _ptr(v_cache), _tag(k_cache) if k_cache.dtype == v_cache.dtype else 0,
+        _arr(k_cache.shape), _arr(k_cache.stride()), _arr(v_cache.stride()),
+        _ptr(kv_page_table), _tag(kv_page_table), kv_page_table.shape[0], kv_page_table.shape[1],
+        kv_page_table.stride(0),
+        _ptr(token_to_request), _tag(token_to_request),
+        _ptr(indices), _tag(indices), width, indices.stride(0),
+        float(scale),
+        _ptr(out), _tag(out), _arr(out.stride()),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(error_word), _stream(stream))
+    _check(st)
+    return out
+
+
+def qsa_decode(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens, query_positions,
+               q_attn, k_cache, v_cache, kv_page_table, scale: float = 1.0 / 16.0,
+               indices=None, out=None, sel_workspace=None, att_workspace=None,
+               error_word=None, stream=None):
+    """One decode step of the whole path: selection then sparse attention on
+    the same stream (the index list stays on the device)."""
+    indices = qsa_select_paged_tokens(q_sel, cmp_cache, cmp_page_table, token_to_request,
+                                      seq_lens, query_positions, out=indices,
+                                      workspace=sel_workspace, error_word=error_word,
+                                      stream=stream)
+    out = qsa_sparse_attention(q_attn, k_cache, v_cache, kv_page_table, token_to_request,
+                               indices, scale=scale, out=out, workspace=att_workspace,
+                               error_word=error_word, stream=stream)
+    return indices, out

@@ -1,0 +1,178 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/qsa.h declares, answers workspace queries, and fails
+closed on bad arguments -- each rejected before any CUDA call, so fake
+(aligned, never dereferenced) device addresses are enough here.  Mirrors the
+fail-closed dtype/layout/output checks of "vLLM: integrate FP16 packed QSA
+extension" (Validation)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_paged_attention_qsa_gb300 as qsa
+from sparse_paged_attention_qsa_gb300 import build as qbuild
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qsa.load_library()
+
+
+def _declared():
+    src = open(HDR).read()
+    return re.findall(r"QSA_API\s+[\w\s\*]+?\b(qsa_\w+)\s*\(", src)
+
+
+def test_header_declares_and_library_exports_every_symbol(lib):
+    names = _declared()
+    assert set(names) == set(qsa.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", qbuild.LIB], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+    # nothing but the ABI leaks out of the library
+    assert {e for e in exported if e.startswith("qsa")} == set(names)
+
+
+def test_header_constants_match_binding():
+    src = open(HDR).read()
+    consts = dict(re.findall(r"#define\s+(QSA_\w+)\s+(\d+)u?\b", src))
+    assert int(consts["QSA_TOKEN_TOPK"]) == qsa.TOKEN_TOPK == 2048
+    assert int(consts["QSA_COMPRESS_RATIO"]) == qsa.COMPRESS_RATIO == 4
+    assert int(consts["QSA_OUT_WIDTH"]) == qsa.OUT_WIDTH == 2051
+    assert int(consts["QSA_TOPK_BLOCKS"]) == qsa.TOPK_BLOCKS == 512
+    assert int(consts["QSA_KV_PAGE_STRIDE"]) == 262144
+    assert int(consts["QSA_V_OFFSET"]) == 256
+    assert int(consts["QSA_DERR_REQUEST"]) == qsa.DERR_REQUEST
+    assert int(consts["QSA_DERR_CMP_PAGE"]) == qsa.DERR_CMP_PAGE
+    assert int(consts["QSA_DERR_KV_PAGE"]) == qsa.DERR_KV_PAGE
+
+
+def test_status_strings_and_version(lib):
+    for s in range(10):
+        assert lib.qsa_status_string(s)
+    assert lib.qsa_status_string(99) == b"unknown status"
+    assert lib.qsa_version() >= 100
+
+
+def test_workspace_queries(lib):
+    assert lib.qsa_select_workspace_bytes(0, 10) == 0
+    assert lib.qsa_select_workspace_bytes(256, 256) == 256 * 256 * 128 * 4
+    assert lib.qsa_select_workspace_bytes(1, 1) % 256 == 0
+    assert lib.qsa_attention_workspace_bytes(0, 2051) == 0
+    a = lib.qsa_attention_workspace_bytes(256, 2051)
+    assert a >= 256 * 3 * 256 * 4 and a % 256 == 0
+    assert lib.qsa_attention_workspace_bytes(1, 0) > 0
+
+
+# --- fail-closed selection --------------------------------------------------
+
+A = 1 << 20          # fake device addresses: distinct, 256-byte aligned
+def _addr(k):
+    return A * (k + 1)
+
+
+def _arr(v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+def _sel(lib, **over):
+    R = over.pop("R", 4)
+    cols = over.pop("cols", 8)
+    a = dict(q=_addr(1), qdt=1, R=R, qs=_arr([512, 128, 1]),
+             cmp=_addr(2), cdt=1, cshape=_arr([64, 128, 1, 128]), cstr=_arr([16384, 128, 128, 1]),
+             pt=_addr(40), ptdt=4, nreq=R, cols=cols, pts0=cols,
+             t2r=_addr(50), t2rdt=4, sl=_addr(60), sldt=4, qp=_addr(70), qpdt=5,
+             topk=2048, ratio=4, out=_addr(80), odt=4, ow=2051, os0=2051,
+             ws=_addr(100), wsb=lib.qsa_select_workspace_bytes(R, cols), err=None, stream=None)
+    a.update(over)
+    return lib.qsa_select_paged_tokens(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(topk=1024), 6), (dict(ratio=8), 6), (dict(ow=2048), 6),
+    (dict(qdt=3), 2), (dict(qdt=2), 2), (dict(cdt=2), 2), (dict(ptdt=5), 2),
+    (dict(t2rdt=5), 2), (dict(sldt=5), 2), (dict(qpdt=4), 2), (dict(odt=5), 2),
+    (dict(R=70000), 3), (dict(R=-1), 3),
+    (dict(cshape=_arr([64, 64, 1, 128])), 3), (dict(cshape=_arr([64, 128, 2, 128])), 3),
+    (dict(cshape=_arr([64, 128, 1, 64])), 3),
+    (dict(qs=_arr([1024, 128, 1])), 4), (dict(qs=_arr([512, 1, 4])), 4),
+    (dict(cstr=_arr([16384 * 2, 128, 128, 1])), 4), (dict(cstr=_arr([16384, 256, 128, 1])), 4),
+    (dict(pts0=4), 4), (dict(os0=2050), 4),
+    (dict(q=None), 1), (dict(cmp=None), 1), (dict(pt=None), 1), (dict(t2r=None), 1),
+    (dict(sl=None), 1), (dict(qp=None), 1), (dict(out=None), 1), (dict(qs=None), 1),
+    (dict(q=_addr(1) + 8), 5), (dict(cmp=_addr(2) + 2), 5), (dict(qp=_addr(70) + 4), 5),
+    (dict(out=_addr(80) + 2), 5), (dict(err=_addr(120) + 1), 5),
+    (dict(ws=None), 7), (dict(wsb=100), 7), (dict(ws=_addr(100) + 16), 5),
+    (dict(out=_addr(1)), 8), (dict(out=_addr(40)), 8), (dict(out=_addr(100)), 8),
+    (dict(err=_addr(80) + 64), 8), (dict(err=_addr(1)), 8),
+])
+def test_select_fails_closed(lib, over, status):
+    assert _sel(lib, **over) == status
+
+
+def test_select_zero_rows_is_noop(lib):
+    assert _sel(lib, R=0, ws=None, wsb=0) == 0
+
+
+# --- fail-closed attention --------------------------------------------------
+
+def _att(lib, **over):
+    R = over.pop("R", 2)
+    W = over.pop("W", 2051)
+    k = over.pop("k", _addr(10))
+    a = dict(q=_addr(1), qdt=1, R=R, qs=_arr([768, 256, 1]),
+             k=k, v=over.pop("v", None if k is None else k + 512), kvdt=1, kvshape=_arr([64, 512, 1, 256]),
+             ks=_arr([262144, 512, 256, 1]), vs=_arr([262144, 512, 256, 1]),
+             pt=_addr(500), ptdt=4, nreq=R, cols=16, pts0=16, t2r=_addr(510), t2rdt=4,
+             idx=_addr(520), idxdt=4, W=W, is0=W, scale=1.0 / 16.0,
+             out=_addr(600), odt=1, os=_arr([768, 256, 1]),
+             ws=_addr(700), wsb=lib.qsa_attention_workspace_bytes(R, W), err=None, stream=None)
+    a.update(over)
+    return lib.qsa_sparse_attention(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qdt=3), 2), (dict(kvdt=2), 2), (dict(odt=3), 2), (dict(ptdt=5), 2),
+    (dict(t2rdt=5), 2), (dict(idxdt=5), 2),
+    (dict(scale=float("nan")), 6), (dict(scale=0.0), 6), (dict(scale=-1.0), 6),
+    (dict(scale=float("inf")), 6), (dict(W=2052, is0=2052), 6),
+    (dict(R=70000), 3), (dict(kvshape=_arr([64, 256, 1, 256])), 3),
+    (dict(kvshape=_arr([64, 512, 2, 256])), 3), (dict(kvshape=_arr([64, 512, 1, 512])), 3),
+    (dict(qs=_arr([768, 1, 3])), 4), (dict(os=_arr([1024, 256, 1])), 4),
+    (dict(ks=_arr([131072, 256, 256, 1])), 4), (dict(vs=_arr([262144, 256, 256, 1])), 4),
+    (dict(ks=_arr([262144, 512, 256, 2])), 4), (dict(v=_addr(10)), 4), (dict(v=_addr(10) + 1024), 4),
+    (dict(pts0=8), 4), (dict(is0=100), 4),
+    (dict(q=None), 1), (dict(k=None, v=None), 1), (dict(pt=None), 1), (dict(t2r=None), 1),
+    (dict(idx=None), 1), (dict(out=None), 1), (dict(ks=None), 1),
+    (dict(q=_addr(1) + 2), 5), (dict(k=_addr(10) + 8), 5), (dict(out=_addr(600) + 8), 5),
+    (dict(idx=_addr(520) + 2), 5),
+    (dict(ws=None), 7), (dict(wsb=16), 7),
+    (dict(out=_addr(1)), 8), (dict(out=_addr(10) + 4096), 8), (dict(out=_addr(520)), 8),
+    (dict(out=_addr(700)), 8), (dict(err=_addr(600)), 8),
+])
+def test_attention_fails_closed(lib, over, status):
+    assert _att(lib, **over) == status
+
+
+def test_attention_zero_rows_and_zero_width(lib):
+    assert _att(lib, R=0, ws=None, wsb=0) == 0
+
+
+def test_binding_raises_without_library(tmp_path):
+    import importlib
+    import sparse_paged_attention_qsa_gb300.binding as b
+    saved = b._lib
+    try:
+        b._lib = None
+        with pytest.raises(RuntimeError, match="not found"):
+            b.load_library(str(tmp_path / "missing.so"))
+    finally:
+        b._lib = saved
