@@ -74,6 +74,7 @@ typedef int qsa_status;
 #define QSA_ERR_WORKSPACE   7  /* workspace missing or too small */
 #define QSA_ERR_ALIAS       8  /* an output overlaps an input */
 #define QSA_ERR_CUDA        9  /* a CUDA runtime call or launch failed */
+#define QSA_ERR_SCRATCH_LIMIT 10 /* request exceeds the static scratch array */
 
 typedef int qsa_dtype;
 #define QSA_DT_F16   1
@@ -194,6 +195,49 @@ QSA_API qsa_status qsa_sparse_attention(
     float scale,
     void* out, qsa_dtype out_dtype, const int64_t out_strides[3],
     void* workspace, size_t workspace_bytes,
+    uint32_t* error_word, qsa_stream_t stream);
+
+/*
+ * qsa_select_paged_tokens_static_scratch -- the same selection, for callers
+ * that cannot give the library a device workspace.  The pages have no
+ * counterpart to this entry point.
+ *
+ * Who needs it: code that cannot allocate device memory where it calls us,
+ * e.g. a plugin that its host framework hands only input and output buffers
+ * (no allocator), or a serving loop that bans cudaMalloc after start-up
+ * because it synchronises the device and may fail under memory pressure.
+ *
+ * Scratch: a fixed array of QSA_STATIC_SCRATCH_BYTES inside the library,
+ * held on every GPU that loads it until the process exits.  A call needs
+ * qsa_select_workspace_bytes(num_rows, cmp_pt_cols) bytes of it; a larger
+ * request returns QSA_ERR_SCRATCH_LIMIT without launching.  The call
+ * allocates nothing.  All calls share the array: calls whose kernels overlap
+ * on the GPU (different streams or host threads) race, so serialise them.
+ * Nothing in the array needs clearing between calls.
+ *
+ * Set-up: the first call with a given device current looks up the array's
+ * device address (cudaGetSymbolAddress) and may load the library's GPU code
+ * onto that device; make that first call before any stream capture.
+ *
+ * Arguments, validation and results are those of qsa_select_paged_tokens
+ * without the workspace pair.
+ */
+#define QSA_STATIC_SCRATCH_BYTES (4u << 20)  /* 4 MiB: 1,048,576 score slots */
+
+QSA_API size_t qsa_static_scratch_bytes(void);
+
+QSA_API qsa_status qsa_select_paged_tokens_static_scratch(
+    const void* q_sel, qsa_dtype q_sel_dtype, int64_t num_rows,
+    const int64_t q_sel_strides[3],
+    const void* cmp_cache, qsa_dtype cmp_dtype, const int64_t cmp_shape[4],
+    const int64_t cmp_strides[4],
+    const void* cmp_page_table, qsa_dtype cmp_pt_dtype, int64_t num_reqs,
+    int64_t cmp_pt_cols, int64_t cmp_pt_stride0,
+    const void* token_to_request, qsa_dtype t2r_dtype,
+    const void* seq_lens, qsa_dtype seq_lens_dtype,
+    const void* query_positions, qsa_dtype qpos_dtype,
+    int32_t token_topk, int32_t compress_ratio,
+    void* out_indices, qsa_dtype out_dtype, int64_t out_width, int64_t out_stride0,
     uint32_t* error_word, qsa_stream_t stream);
 
 #ifdef __cplusplus

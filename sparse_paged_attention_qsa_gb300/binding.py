@@ -31,11 +31,13 @@ _DTYPE_TAG = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_
 
 STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE",
           4: "QSA_ERR_STRIDE", 5: "QSA_ERR_ALIGN", 6: "QSA_ERR_CONTRACT",
-          7: "QSA_ERR_WORKSPACE", 8: "QSA_ERR_ALIAS", 9: "QSA_ERR_CUDA"}
+          7: "QSA_ERR_WORKSPACE", 8: "QSA_ERR_ALIAS", 9: "QSA_ERR_CUDA",
+          10: "QSA_ERR_SCRATCH_LIMIT"}
 
 EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
-            "qsa_sparse_attention")
+            "qsa_sparse_attention", "qsa_static_scratch_bytes",
+            "qsa_select_paged_tokens_static_scratch")
 
 
 class QSAError(RuntimeError):

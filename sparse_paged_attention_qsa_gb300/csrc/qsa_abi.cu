@@ -50,6 +50,8 @@ const char* qsa_status_string(qsa_status s) {
     case QSA_ERR_WORKSPACE: return "workspace missing or too small";
     case QSA_ERR_ALIAS: return "output overlaps an input";
     case QSA_ERR_CUDA: return "CUDA launch failed";
+    case QSA_ERR_SCRATCH_LIMIT:
+      return "request exceeds the static scratch array (use qsa_select_paged_tokens with a workspace)";
     default: return "unknown status";
   }
 }
