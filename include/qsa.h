@@ -90,6 +90,8 @@ typedef int qsa_dtype;
                                   block lies beyond the page-table columns */
 #define QSA_DERR_KV_PAGE   4u  /* K/V page id negative / >= P_kv, or the
                                   index lies beyond the page-table columns */
+#define QSA_DERR_TIMEOUT   8u  /* a device-side wait exceeded its 1 s bound;
+                                  the call's outputs are not valid */
 
 typedef struct CUstream_st* qsa_stream_t;  /* == cudaStream_t; NULL = legacy */
 

@@ -23,7 +23,7 @@ TOKEN_TOPK = 2048
 COMPRESS_RATIO = 4
 TOPK_BLOCKS = 512
 OUT_WIDTH = 2051
-DERR_REQUEST, DERR_CMP_PAGE, DERR_KV_PAGE = 1, 2, 4
+DERR_REQUEST, DERR_CMP_PAGE, DERR_KV_PAGE, DERR_TIMEOUT = 1, 2, 4, 8
 
 DT_F16, DT_BF16, DT_F32, DT_I32, DT_I64 = 1, 2, 3, 4, 5
 _DTYPE_TAG = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_F32,

@@ -91,6 +91,10 @@ qsa_status qsa_select_paged_tokens(
       cmp_shape[3] != kSelDim)
     return QSA_ERR_SHAPE;
   if (num_reqs < 0 || cmp_pt_cols < 0) return QSA_ERR_SHAPE;
+  // the streaming loads address page p at row 256*p of a 32-bit row space;
+  // per-launch page counts are 32-bit (at most 2^20 pages per request)
+  if (cmp_shape[0] > (int64_t)(INT32_MAX / (2 * kCmpPageKeys))) return QSA_ERR_SHAPE;
+  if (cmp_pt_cols > (int64_t)1 << 20) return QSA_ERR_SHAPE;
   if (num_rows == 0) return QSA_OK;
   if (num_reqs == 0 || cmp_pt_cols == 0) return QSA_ERR_SHAPE;
   // strides: q contiguous [R,4,128]; cache pages [P,128,1,128] contiguous

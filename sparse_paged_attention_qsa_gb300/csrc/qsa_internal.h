@@ -29,6 +29,7 @@ constexpr int kKvTokenHalves = 512;
 constexpr uint32_t kErrRequest = 1u;
 constexpr uint32_t kErrCmpPage = 2u;
 constexpr uint32_t kErrKvPage = 4u;
+constexpr uint32_t kErrTimeout = 8u;
 
 struct SelectParams {
   const __half* q_sel;        // [R,4,128]

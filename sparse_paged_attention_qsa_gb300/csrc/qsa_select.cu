@@ -8,9 +8,11 @@
 // _build_qsa_metadata_kernel: max(0, min((pos+1)//4, seq_len//4)).
 //
 // Two kernels on the caller's stream:
-//   score_kernel  streams every visible compressed key of every row once
-//                 (the dominant HBM stream: 256 B per key) and writes a 32-bit
-//                 ordered score key per block to the workspace;
+//   score_kernel  persistent (one CTA per SM): streams every visible
+//                 compressed page of every row once through a TMA ring in
+//                 shared memory (the dominant HBM stream: 256 B per key) and
+//                 writes a 32-bit ordered score key per block to the
+//                 workspace;
 //   topk_kernel   one CTA per row: exact radix select of the top-512 keys over
 //                 the row's scores (L2-resident), bitonic sort of the winners,
 //                 expansion, tail and -1 padding.
@@ -24,13 +26,24 @@
 #include "qsa_internal.h"
 #include "qsa_device.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 namespace qsa {
 namespace {
 
-constexpr int kScoreThreads = 256;                 // 8 warps
-constexpr int kKeysPerWarpIter = 8;                // 4 lanes per key
-constexpr int kScoreIters = 4;
-constexpr int kKeysPerCta = (kScoreThreads / 32) * kKeysPerWarpIter * kScoreIters;  // 256
+// score kernel: persistent, one CTA per SM, warp-specialised
+constexpr int kStages = 6;                              // 6 x 32 KiB pages in flight per SM
+constexpr int kPageBytes = kCmpPageKeys * kSelDim * 2;  // one compressed page
+constexpr int kScoreWarps = 8;                          // 16 keys of a page per warp
+constexpr int kScoreThreads = kScoreWarps * 32;
+constexpr int kMaxRows = 2048;                          // rows per launch (row tables in smem)
+constexpr size_t kScoreSmem = (size_t)kStages * kPageBytes + 1024 + 2 * kStages * 8 +
+                              kStages * 16 + 3 * kMaxRows * sizeof(int);
+constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s: any wait longer is a fault
 
 constexpr int kTopkThreads = 512;
 
@@ -56,88 +69,362 @@ __device__ __forceinline__ RowSetup row_setup(const SelectParams& p, int r) {
   return s;
 }
 
-__global__ void __launch_bounds__(kScoreThreads)
-score_kernel(const SelectParams p) {
-  const int r = blockIdx.y;
-  const RowSetup rs = row_setup(p, r);
-  if (!rs.ok) return;
-  const int64_t Vs = rs.V < p.vcap ? rs.V : p.vcap;
-  const int64_t cta_base = (int64_t)blockIdx.x * kKeysPerCta;
-  if (cta_base >= Vs) return;
+// --- mbarrier / TMA helpers (sm_90+ PTX) -------------------------------------
 
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int t = lane & 3;          // 32-dim slice of the key
-  const int kslot = lane >> 2;     // key within the warp's group of 8
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of the given parity to complete; gives up after
+// kWaitLimitNs (returns false) so a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t mbar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
 
-  // query slice [32t, 32t+32) of each head, as (even, odd) binary32 pairs
-  float2 q[kSelHeads][16];
-  {
-    const uint4* qp = reinterpret_cast<const uint4*>(p.q_sel + (int64_t)r * kSelHeads * kSelDim);
+// acc + a*b with fp16 operands and a binary32 accumulator (one rounding; the
+// fp16 x fp16 product is exact in binary32, so this equals the fp32 chain step)
+__device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float c) {
+  float d;
+  if (hi)
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
+        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+  else
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
+        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+  return d;
+}
+
+// Score of one key held as four 32-dim slices by a quad of lanes, reduced in
+// the canonical order; returns the ordered key bits(s)+1 on every lane.
+// q: this lane's slice of the 4 heads as fp16 pairs (dims 32t+2j, 32t+2j+1);
+// kv: the key's slice as 4 x 16 bytes.
+__device__ __forceinline__ uint32_t quad_score(const uint32_t (&q)[kSelHeads][16],
+                                               const uint4 (&kv)[4], int t) {
+  float E[kSelHeads], O[kSelHeads];
 #pragma unroll
-    for (int h = 0; h < kSelHeads; ++h) {
+  for (int h = 0; h < kSelHeads; ++h) E[h] = O[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 v = qp[h * 16 + t * 4 + i];
-        q[h][4 * i + 0] = h2f2(v.x);
-        q[h][4 * i + 1] = h2f2(v.y);
-        q[h][4 * i + 2] = h2f2(v.z);
-        q[h][4 * i + 3] = h2f2(v.w);
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+      for (int h = 0; h < kSelHeads; ++h) {
+        E[h] = fma_h(q[h][4 * i + m], w[m], false, E[h]);   // even dims
+        O[h] = fma_h(q[h][4 * i + m], w[m], true, O[h]);    // odd dims
       }
     }
   }
-  const int32_t* ptrow = p.pt + (int64_t)rs.req * p.pt_stride0;
-  uint32_t* srow = p.scores + (int64_t)r * p.vcap;
-
-#pragma unroll 1
-  for (int it = 0; it < kScoreIters; ++it) {
-    const int64_t b = cta_base + warp * (kKeysPerWarpIter * kScoreIters) + it * kKeysPerWarpIter + kslot;
-    const bool inb = b < Vs;
-    bool valid = false;
-    uint4 kv[4] = {};
-    if (inb) {
-      const int32_t pg = ptrow[b >> 7];
-      valid = pg >= 0 && pg < p.num_pages;
-      if (valid) {
-        const __half* kp = p.cmp + (int64_t)pg * kCmpPageHalves + (b & 127) * kSelDim + 32 * t;
+  float P[kSelHeads];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) kv[i] = ld_stream16(kp + 8 * i);
-      } else if (t == 0) {
-        report(p.err, kErrCmpPage);
+  for (int h = 0; h < kSelHeads; ++h) P[h] = __fadd_rn(E[h], O[h]);   // P_t = E_t + O_t
+  // reduce-scatter over the quad: lanes t, t^2 (slices 0+2, 1+3), then t^1;
+  // lane t ends with head t's d = (P0 + P2) + (P1 + P3)
+  const bool hi2 = (t & 2) != 0;
+  const float send0 = hi2 ? P[0] : P[2];
+  const float send1 = hi2 ? P[1] : P[3];
+  const float keep0 = hi2 ? P[2] : P[0];
+  const float keep1 = hi2 ? P[3] : P[1];
+  const float A0 = __fadd_rn(keep0, __shfl_xor_sync(0xffffffffu, send0, 2));
+  const float A1 = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 2));
+  const bool hi1 = (t & 1) != 0;
+  const float d = __fadd_rn(hi1 ? A1 : A0, __shfl_xor_sync(0xffffffffu, hi1 ? A0 : A1, 1));
+  const float rho = d > 0.f ? d : 0.f;
+  const float u = __fadd_rn(rho, __shfl_xor_sync(0xffffffffu, rho, 1));
+  const float s = __fadd_rn(u, __shfl_xor_sync(0xffffffffu, u, 2));  // (r0+r1)+(r2+r3)
+  return __float_as_uint(s) + 1u;
+}
+
+struct StageDesc {
+  int row;        // -1: no more work
+  int b0;         // first block of the page
+  int nkeys;      // visible keys in the page (<= 128)
+  int pad;
+};
+
+// Persistent streaming score kernel over rows [0, p.R) (p.R <= kMaxRows).
+//
+// Prologue: every CTA computes each row's visible-page count and their
+// prefix sum in shared memory, so the W = sum of pages can be cut into
+// equal contiguous ranges, one per CTA (pages of one row are consecutive,
+// so a CTA changes rows rarely and reads consecutive page-table entries).
+//
+// Main loop: thread 0 walks its range and streams each page (32 KiB =
+// 128 keys x two 128-byte rows) into a ring of shared-memory stages with one
+// 2-D TMA load (128-byte swizzle, L2 evict-first), writing a small stage
+// descriptor (row, first block, key count) before arming the stage; it keeps
+// up to kStages pages in flight and blocks only for the stage this CTA is
+// about to consume.  All eight warps score 16 keys of each page.  With the
+// swizzle, lane (key k, slice t) reads row 2k + t/2, 16-byte chunks
+// (4(t&1)+j) XOR (row & 7): the 8 lanes of each shared-memory phase hit 8
+// distinct bank groups, and each lane reads its slice in ascending order.
+__global__ void __launch_bounds__(kScoreThreads, 1)
+score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ int s_abort;
+  __shared__ int64_t s_total;
+  __shared__ int warp_sum[kScoreWarps];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  const uint32_t base = raw + pad;
+  const uint32_t bar_full = base + kStages * kPageBytes;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+  unsigned char* gbase = smem_raw + pad;
+  StageDesc* desc = reinterpret_cast<StageDesc*>(gbase + kStages * kPageBytes + 2 * kStages * 8);
+  int* row_req = reinterpret_cast<int*>(desc + kStages);
+  int* row_vs = row_req + kMaxRows;
+  int* row_pre = row_vs + kMaxRows;          // exclusive prefix of page counts
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const bool producer = tid == 0;
+
+  if (producer) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kScoreWarps);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+
+  // ---- prologue: per-row visible pages and their prefix sum ----
+  constexpr int kRowsPerThread = kMaxRows / kScoreThreads;
+  int cnt[kRowsPerThread];
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) {
+    const int r = tid * kRowsPerThread + i;
+    cnt[i] = 0;
+    if (r < p.R) {
+      const RowSetup rs = row_setup(p, r);
+      const int64_t Vs = rs.ok ? (rs.V < p.vcap ? rs.V : p.vcap) : 0;
+      row_req[r] = rs.ok ? rs.req : -1;
+      row_vs[r] = (int)Vs;
+      cnt[i] = (int)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
+    }
+    mine += cnt[i];
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  int64_t tot = 0;
+  for (int w = 0; w < kScoreWarps; ++w) {
+    before += (w < warp) ? warp_sum[w] : 0;
+    tot += warp_sum[w];
+  }
+  int run = before + incl - mine;
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) {
+    const int r = tid * kRowsPerThread + i;
+    if (r < p.R) row_pre[r] = run;
+    run += cnt[i];
+  }
+  if (tid == 0) s_total = tot;
+  __syncthreads();
+
+  const int64_t W = s_total;
+  const int64_t w_begin = W * blockIdx.x / gridDim.x;
+  const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
+  volatile int* abort_flag = &s_abort;
+
+  // producer state (thread 0 only)
+  int64_t issued = 0;
+  int64_t pw = w_begin;
+  int prow = 0, pcol = 0;
+  bool ended = false;
+  uint64_t policy = 0;
+  if (producer) {
+    policy = evict_first_policy();
+    if (pw < w_end) {   // row holding page pw: last r with row_pre[r] <= pw and pages left
+      int lo = 0, hi = p.R - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (row_pre[mid] <= pw) lo = mid; else hi = mid - 1;
+      }
+      prow = lo;
+      // rows with no pages share the prefix of the next row: step past them
+      while (row_pre[prow] + (int64_t)((row_vs[prow] + kCmpPageKeys - 1) / kCmpPageKeys) <= pw) ++prow;
+      pcol = (int)(pw - row_pre[prow]);
+    }
+  }
+
+  const int t = lane & 3;          // 32-dim slice of the key
+  const int kslot = lane >> 2;     // key within a group of 8
+  uint32_t q[kSelHeads][16];
+  int loaded_row = -1;
+  uint32_t* srow = nullptr;
+  int64_t used = 0;                // stages consumed
+
+  for (;;) {
+    // ---- keep the ring full (thread 0) ----
+    if (producer) {
+      while (!ended && issued < used + kStages && !*abort_flag) {
+        const int s = (int)(issued % kStages);
+        const uint32_t ph = (uint32_t)((issued / kStages) & 1);
+        if (issued >= kStages) {
+          if (issued == used) {
+            if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
+              *abort_flag = 1;
+              report(p.err, kErrTimeout);
+              break;
+            }
+          } else if (!mbar_try_wait(bar_empty + 8 * s, ph ^ 1u)) {
+            break;
+          }
+        }
+        // next page with a loadable physical page (zero-fill the others)
+        int32_t pg = -1;
+        while (pw < w_end) {
+          const int req = row_req[prow];
+          const int vs = row_vs[prow];
+          const int b0 = pcol * kCmpPageKeys;
+          pg = __ldg(p.pt + (int64_t)req * p.pt_stride0 + pcol);
+          const int nk = vs - b0 < kCmpPageKeys ? vs - b0 : kCmpPageKeys;
+          const int row = prow;
+          ++pw;
+          if (++pcol * kCmpPageKeys >= vs) {
+            pcol = 0;
+            ++prow;
+            while (prow < p.R && row_vs[prow] == 0) ++prow;
+          }
+          if (pg >= 0 && pg < p.num_pages) {
+            desc[s].row = row;
+            desc[s].b0 = b0;
+            desc[s].nkeys = nk;
+            break;
+          }
+          uint32_t* zr = p.scores + (int64_t)row * p.vcap + b0;   // no key for these blocks
+          for (int k = 0; k < nk; ++k) zr[k] = 0u;
+          report(p.err, kErrCmpPage);
+          pg = -1;
+        }
+        if (pg >= 0) {
+          mbar_expect_tx(bar_full + 8 * s, kPageBytes);
+          tma_load_2d(base + s * kPageBytes, &tmap, 0, pg * 2 * kCmpPageKeys, bar_full + 8 * s,
+                      policy);
+        } else {                    // range done: mark the stage as the end
+          desc[s].row = -1;
+          mbar_arrive(bar_full + 8 * s);
+          ended = true;
+        }
+        ++issued;
       }
     }
-    float2 acc[kSelHeads];
+    __syncwarp();
+    if (*abort_flag) break;
+
+    const int s = (int)(used % kStages);
+    const uint32_t ph = (uint32_t)((used / kStages) & 1);
+    if (!mbar_wait(bar_full + 8 * s, ph)) {
+      *abort_flag = 1;
+      report(p.err, kErrTimeout);
+      break;
+    }
+    const StageDesc d = desc[s];
+    if (d.row < 0) break;
+    if (d.row != loaded_row) {
+      loaded_row = d.row;
+      srow = p.scores + (int64_t)d.row * p.vcap;
+      // query slice [32t, 32t+32) of each head, fp16 pairs
+      const uint4* qp = reinterpret_cast<const uint4*>(p.q_sel + (int64_t)d.row * kSelHeads * kSelDim);
 #pragma unroll
-    for (int h = 0; h < kSelHeads; ++h) acc[h] = make_float2(0.f, 0.f);
+      for (int h = 0; h < kSelHeads; ++h) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t w[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float2 kf = h2f2(w[m]);
-#pragma unroll
-        for (int h = 0; h < kSelHeads; ++h) acc[h] = ffma2(q[h][4 * i + m], kf, acc[h]);
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = qp[h * 16 + t * 4 + i];
+          q[h][4 * i + 0] = v.x;
+          q[h][4 * i + 1] = v.y;
+          q[h][4 * i + 2] = v.z;
+          q[h][4 * i + 3] = v.w;
+        }
       }
     }
-    float P[kSelHeads];
+    const uint32_t stage = base + s * kPageBytes;
+    uint4 kv[2][4];
 #pragma unroll
-    for (int h = 0; h < kSelHeads; ++h) P[h] = __fadd_rn(acc[h].x, acc[h].y);
-
-    // quad reduce-scatter: lanes t, t^2 first (slices 0+2, 1+3), then t^1;
-    // lane t ends with head t's d = (P0 + P2) + (P1 + P3).
-    const bool hi2 = (t & 2) != 0;
-    const float send0 = hi2 ? P[0] : P[2];
-    const float send1 = hi2 ? P[1] : P[3];
-    const float keep0 = hi2 ? P[2] : P[0];
-    const float keep1 = hi2 ? P[3] : P[1];
-    const float A0 = __fadd_rn(keep0, __shfl_xor_sync(0xffffffffu, send0, 2));
-    const float A1 = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 2));
-    const bool hi1 = (t & 1) != 0;
-    const float d = __fadd_rn(hi1 ? A1 : A0, __shfl_xor_sync(0xffffffffu, hi1 ? A0 : A1, 1));
-    const float rho = d > 0.f ? d : 0.f;
-    const float u = __fadd_rn(rho, __shfl_xor_sync(0xffffffffu, rho, 1));
-    const float s = __fadd_rn(u, __shfl_xor_sync(0xffffffffu, u, 2));
-    if (inb && t == 0) srow[b] = valid ? (__float_as_uint(s) + 1u) : 0u;
+    for (int g = 0; g < 2; ++g) {
+      const int k = warp * 16 + g * 8 + kslot;
+      const uint32_t row = 2 * k + (t >> 1);
+      const uint32_t rbase = stage + row * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
+        kv[g][j] = lds128(rbase + chunk * 16);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const uint32_t key = quad_score(q, kv[g], t);
+      const int k = warp * 16 + g * 8 + kslot;
+      if (t == 0 && k < d.nkeys) srow[d.b0 + k] = key;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
+    ++used;
+  }
+  __syncthreads();
+  // After a timeout, let every copy this CTA issued land before it exits.
+  if (*abort_flag && producer) {
+    const int64_t first = issued > kStages ? issued - kStages : 0;
+    for (int64_t n = first; n < issued; ++n)
+      mbar_wait(bar_full + 8 * (int)(n % kStages), (uint32_t)((n / kStages) & 1));
   }
 }
 
@@ -293,14 +580,89 @@ size_t select_workspace_bytes(int64_t R, int64_t pt_cols) {
   return (n + 255) & ~(size_t)255;
 }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D view of the compressed cache: rows of 64 halves (128 B), two rows per
+// key, 256 rows per page; one box = one page; 128-byte swizzle.
+cudaError_t encode_cmp_map(const SelectParams& p, CUtensorMap* map) {
+  memset(map, 0, sizeof(*map));
+  if (p.num_pages <= 0) return cudaSuccess;   // no page can be loaded
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {64, (cuuint64_t)p.num_pages * 2 * kCmpPageKeys};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, 2 * kCmpPageKeys};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(p.cmp), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool smem_set = false;
+};
+
+cudaError_t device_info(DeviceInfo** out) {
+  static std::mutex mu;
+  static DeviceInfo info[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = info[dev];
+  if (!d.smem_set) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScoreSmem);
+    if (e != cudaSuccess) return e;
+    d.smem_set = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
-  const int64_t ctas = (p.vcap + kKeysPerCta - 1) / kKeysPerCta;
-  if (ctas > 0) {
-    dim3 grid((unsigned)ctas, (unsigned)p.R);
-    score_kernel<<<grid, kScoreThreads, 0, stream>>>(p);
+  DeviceInfo* di = nullptr;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  CUtensorMap map;
+  e = encode_cmp_map(p, &map);
+  if (e != cudaSuccess) return e;
+  // rows in chunks of kMaxRows (the score kernel keeps per-row tables in smem)
+  for (int r0 = 0; r0 < p.R; r0 += kMaxRows) {
+    SelectParams c = p;
+    c.R = p.R - r0 < kMaxRows ? p.R - r0 : kMaxRows;
+    c.q_sel = p.q_sel + (int64_t)r0 * kSelHeads * kSelDim;
+    c.t2r = p.t2r + r0;
+    c.qpos = p.qpos + r0;
+    c.out = p.out + (int64_t)r0 * p.out_stride0;
+    c.scores = p.scores + (int64_t)r0 * p.vcap;
+    const int64_t items = (int64_t)c.R * c.pt_cols;
+    const int grid = (int)(items < di->sms ? items : di->sms);
+    score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
+    topk_kernel<<<c.R, kTopkThreads, 0, stream>>>(c);
   }
-  topk_kernel<<<p.R, kTopkThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
