@@ -178,6 +178,8 @@ qsa_status qsa_sparse_attention(
       kv_shape[3] != kAttDim)
     return QSA_ERR_SHAPE;
   if (num_reqs < 0 || kv_pt_cols < 0) return QSA_ERR_SHAPE;
+  // tokens are addressed as 32-bit page*512 + slot
+  if (kv_shape[0] > (int64_t)(UINT32_MAX / qsa::kKvPageTokens)) return QSA_ERR_SHAPE;
   if (num_rows == 0) return QSA_OK;
   if (num_reqs == 0 || kv_pt_cols == 0) return QSA_ERR_SHAPE;
   if (q_strides[0] != kAttHeads * kAttDim || q_strides[1] != kAttDim || q_strides[2] != 1)

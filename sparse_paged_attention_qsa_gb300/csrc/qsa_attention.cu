@@ -8,13 +8,15 @@
 //
 // Split-width flash decoding:
 //   attn_partial_kernel  grid (splits, R); each CTA takes kSplit consecutive
-//                        entries of one row's index list; each warp walks 32
-//                        of them.  Lane l owns dims [8l, 8l+8) of K and V, so
-//                        a token's 1 KiB (K then V) is read as two coalesced
-//                        512-byte warp loads.  Logits use an online softmax in
-//                        base 2 (q is pre-scaled by scale*log2 e); the four
-//                        warps merge in shared memory and the CTA writes one
-//                        partial (m, l, acc[256]) per head to the workspace.
+//                        entries of one row's index list; each warp compacts
+//                        its 32 entries to the valid tokens and walks them 8
+//                        at a time (8 KiB of K/V in flight per warp).  Logits
+//                        (mixed-precision FMA, fp16 operands, binary32
+//                        accumulation) are reduced with one warp
+//                        reduce-scatter per batch; the online softmax runs in
+//                        base 2.  The four warps merge in shared memory and
+//                        the CTA writes one partial (m, l, acc[256]) per head
+//                        to the workspace.
 //   attn_combine_kernel  one CTA per row merges the splits by log-sum-exp and
 //                        rounds to FP16 (nearest even).  No valid entry -> 0.
 #include "qsa_internal.h"
@@ -26,8 +28,24 @@ namespace qsa {
 namespace {
 
 constexpr int kSplit = 128;          // index entries per CTA
-constexpr int kAttThreads = 128;     // 4 warps x 32 entries
+constexpr int kAttWarps = 4;         // 32 entries per warp
+constexpr int kAttThreads = kAttWarps * 32;
+constexpr int kBatch = 8;            // tokens per warp step
 constexpr int kPartFloats = kAttHeads * 2 + kAttHeads * kAttDim;   // m[3], l[3], acc[3][256]
+
+// acc + a*b with fp16 operands and a binary32 accumulator
+__device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float c) {
+  float d;
+  if (hi)
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
+        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+  else
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
+        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ void to_f32x8(const uint4 v, float* f) {
   const float2 a = h2f2(v.x), b = h2f2(v.y), c = h2f2(v.z), d = h2f2(v.w);
@@ -35,6 +53,32 @@ __device__ __forceinline__ void to_f32x8(const uint4 v, float* f) {
   f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+// Sum 32 per-lane values over the warp, reduce-scatter style: on return
+// x[0] of lane l holds the warp-wide sum of value l (31 shuffles).
+__device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int level = 0; level < 5; ++level) {
+    const int half = 16 >> level;            // values kept after this level
+    const int bit = 16 >> level;             // partner lane distance
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? x[i] : x[i + half];
+      const float keep = upper ? x[i + half] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+  return x[0];
+}
+
+// One CTA = kSplit consecutive entries of one row's index list; each warp
+// takes 32 of them, compacts the valid ones (holes and unmapped pages
+// dropped) and walks them kBatch tokens at a time.  Lane l owns dims
+// [8l, 8l+8) of K and V, so a token's 1 KiB (K then V) is two coalesced
+// 512-byte warp loads; a batch keeps 8 KiB in flight per warp.  The 24 head
+// logits of a batch are reduced with one reduce-scatter, after which lane l
+// holds token l/4, head l%4 (head 3 is padding); the online softmax runs in
+// base 2 with one exp2 per lane per batch.
 __global__ void __launch_bounds__(kAttThreads)
 attn_partial_kernel(const AttentionParams p) {
   const int split = blockIdx.x;
@@ -43,95 +87,135 @@ attn_partial_kernel(const AttentionParams p) {
   const int lane = tid & 31;
   const int warp = tid >> 5;
 
-  __shared__ float sm_m[4][kAttHeads], sm_l[4][kAttHeads];
-  __shared__ float sm_acc[4][kAttHeads][kAttDim];
+  __shared__ float sm_m[kAttWarps][kAttHeads], sm_l[kAttWarps][kAttHeads];
+  __shared__ float sm_acc[kAttWarps][kAttHeads][kAttDim];
+  __shared__ uint32_t sm_tok[kAttWarps][32];
 
   const int req = p.t2r[r];
   const bool rok = req >= 0 && req < p.num_reqs;
   if (!rok && split == 0 && tid == 0) report(p.err, kErrRequest);
 
-  // query dims [8*lane, 8*lane+8) of each head, scaled to base-2 logits
-  float qf[kAttHeads][8];
+  // query dims [8*lane, 8*lane+8) of each head, fp16 pairs
+  uint32_t qh[kAttHeads][4];
   {
     const uint4* qp = reinterpret_cast<const uint4*>(p.q + (int64_t)r * kAttHeads * kAttDim);
 #pragma unroll
     for (int h = 0; h < kAttHeads; ++h) {
-      to_f32x8(qp[h * 32 + lane], qf[h]);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) qf[h][d] *= p.scale_log2;
+      const uint4 v = qp[h * 32 + lane];
+      qh[h][0] = v.x; qh[h][1] = v.y; qh[h][2] = v.z; qh[h][3] = v.w;
     }
   }
 
-  // resolve this lane's entry to a token address (or a hole)
+  // resolve this lane's entry to a token (page*512 + slot) or a hole
   const int64_t j = (int64_t)split * kSplit + warp * 32 + lane;
-  const __half* tok = nullptr;
+  bool valid = false;
+  uint32_t tok = 0;
   if (rok && j < p.width) {
     const int32_t i = p.idx[(int64_t)r * p.idx_stride0 + j];
     if (i >= 0) {
       const int64_t col = i >> 9;
-      bool ok = col < p.pt_cols;
       int32_t pg = -1;
-      if (ok) {
-        pg = p.pt[(int64_t)req * p.pt_stride0 + col];
-        ok = pg >= 0 && pg < p.num_pages;
+      if (col < p.pt_cols) pg = p.pt[(int64_t)req * p.pt_stride0 + col];
+      if (pg >= 0 && pg < p.num_pages) {
+        valid = true;
+        tok = (uint32_t)pg * kKvPageTokens + (uint32_t)(i & 511);
+      } else {
+        report(p.err, kErrKvPage);
       }
-      if (ok) tok = p.kv + (int64_t)pg * kKvPageHalves + (int64_t)(i & 511) * kKvTokenHalves;
-      else report(p.err, kErrKvPage);
     }
   }
-  unsigned vmask = __ballot_sync(0xffffffffu, tok != nullptr);
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  const int nvalid = __popc(vmask);
+  if (valid) sm_tok[warp][__popc(vmask & ((1u << lane) - 1u))] = tok;
+  __syncwarp();
 
-  float m[kAttHeads], l[kAttHeads], acc[kAttHeads][8];
+  const int hh = lane & 3;         // head of this lane's logit after the reduce
+  float m_run = -CUDART_INF_F, l_run = 0.f;
+  float acc[kAttHeads][8];
 #pragma unroll
-  for (int h = 0; h < kAttHeads; ++h) {
-    m[h] = -CUDART_INF_F;
-    l[h] = 0.f;
+  for (int h = 0; h < kAttHeads; ++h)
 #pragma unroll
     for (int d = 0; d < 8; ++d) acc[h][d] = 0.f;
+
+  for (int b0 = 0; b0 < nvalid; b0 += kBatch) {
+    uint4 kr[kBatch], vr[kBatch];
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      if (b0 + t < nvalid) {
+        const __half* tp = p.kv + (int64_t)sm_tok[warp][b0 + t] * kKvTokenHalves;
+        kr[t] = ld_stream16(tp + 8 * lane);
+        vr[t] = ld_stream16(tp + kAttDim + 8 * lane);
+      } else {
+        kr[t] = make_uint4(0, 0, 0, 0);
+        vr[t] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // partial logits over this lane's 8 dims: x[4t + h]
+    float x[32];
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      const uint32_t w[4] = {kr[t].x, kr[t].y, kr[t].z, kr[t].w};
+#pragma unroll
+      for (int h = 0; h < kAttHeads; ++h) {
+        float a = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          a = fma_h(qh[h][m], w[m], false, a);
+          a = fma_h(qh[h][m], w[m], true, a);
+        }
+        x[4 * t + h] = a;
+      }
+      x[4 * t + 3] = 0.f;
+    }
+    const float dot = reduce_scatter32(x, lane);
+    const int tt = lane >> 2;
+    const bool live = hh < kAttHeads && b0 + tt < nvalid;
+    const float z = live ? dot * p.scale_log2 : -CUDART_INF_F;
+    // batch max per head over the 8 tokens (lanes with the same l%4)
+    float mb = z;
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+    const float m_new = fmaxf(m_run, mb);
+    const bool any = m_new != -CUDART_INF_F;
+    const float c = any ? exp2f(m_run - m_new) : 1.f;
+    const float pz = any ? exp2f(z - m_new) : 0.f;
+    float ps = pz;
+    ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    l_run = fmaf(l_run, c, ps);
+    m_run = m_new;
+    // P.V over the batch: every lane needs all 24 weights and 3 scales
+    float ch[kAttHeads];
+#pragma unroll
+    for (int h = 0; h < kAttHeads; ++h) ch[h] = __shfl_sync(0xffffffffu, c, h);
+#pragma unroll
+    for (int h = 0; h < kAttHeads; ++h)
+#pragma unroll
+      for (int d = 0; d < 8; ++d) acc[h][d] *= ch[h];
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      float vf[8];
+      to_f32x8(vr[t], vf);
+#pragma unroll
+      for (int h = 0; h < kAttHeads; ++h) {
+        const float pw = __shfl_sync(0xffffffffu, pz, 4 * t + h);
+#pragma unroll
+        for (int d = 0; d < 8; ++d) acc[h][d] = fmaf(pw, vf[d], acc[h][d]);
+      }
+    }
   }
 
-  while (vmask) {
-    const int src = __ffs(vmask) - 1;
-    vmask &= vmask - 1;
-    const unsigned long long a =
-        __shfl_sync(0xffffffffu, (unsigned long long)tok, src);
-    const __half* tp = reinterpret_cast<const __half*>(a);
-    const uint4 kraw = ld_stream16(tp + 8 * lane);
-    const uint4 vraw = ld_stream16(tp + kAttDim + 8 * lane);
-    float kf[8], vf[8];
-    to_f32x8(kraw, kf);
-    to_f32x8(vraw, vf);
-    float z[kAttHeads];
-#pragma unroll
-    for (int h = 0; h < kAttHeads; ++h) {
-      float s = 0.f;
-#pragma unroll
-      for (int d = 0; d < 8; ++d) s = fmaf(qf[h][d], kf[d], s);
-      z[h] = s;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-      for (int h = 0; h < kAttHeads; ++h) z[h] += __shfl_xor_sync(0xffffffffu, z[h], o);
-    }
-#pragma unroll
-    for (int h = 0; h < kAttHeads; ++h) {
-      const float mn = fmaxf(m[h], z[h]);
-      const float c = exp2f(m[h] - mn);
-      const float pz = exp2f(z[h] - mn);
-      l[h] = fmaf(l[h], c, pz);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) acc[h][d] = fmaf(acc[h][d], c, pz * vf[d]);
-      m[h] = mn;
-    }
-  }
-
-  // merge the four warps
+  // merge the four warps (lane h holds head h's m and l)
 #pragma unroll
   for (int h = 0; h < kAttHeads; ++h) {
 #pragma unroll
     for (int d = 0; d < 8; ++d) sm_acc[warp][h][8 * lane + d] = acc[h][d];
-    if (lane == 0) { sm_m[warp][h] = m[h]; sm_l[warp][h] = l[h]; }
+  }
+  if (lane < kAttHeads) {
+    sm_m[warp][lane] = m_run;
+    sm_l[warp][lane] = l_run;
   }
   __syncthreads();
   float* part = p.part + ((int64_t)r * p.nsplit + split) * kPartFloats;
@@ -139,14 +223,14 @@ attn_partial_kernel(const AttentionParams p) {
     const int h = o / kAttDim, d = o % kAttDim;
     float M = sm_m[0][h];
 #pragma unroll
-    for (int w = 1; w < 4; ++w) M = fmaxf(M, sm_m[w][h]);
+    for (int w = 1; w < kAttWarps; ++w) M = fmaxf(M, sm_m[w][h]);
     float A = 0.f, Lsum = 0.f;
     if (M != -CUDART_INF_F) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float c = exp2f(sm_m[w][h] - M);
-        A = fmaf(c, sm_acc[w][h][d], A);
-        Lsum = fmaf(c, sm_l[w][h], Lsum);
+      for (int w = 0; w < kAttWarps; ++w) {
+        const float cw = exp2f(sm_m[w][h] - M);
+        A = fmaf(cw, sm_acc[w][h][d], A);
+        Lsum = fmaf(cw, sm_l[w][h], Lsum);
       }
     }
     part[kAttHeads * 2 + o] = A;
@@ -157,27 +241,54 @@ attn_partial_kernel(const AttentionParams p) {
   }
 }
 
+constexpr int kMaxSplits = (kOutWidth + kSplit - 1) / kSplit;   // 17
+
+// One CTA per row: log-sum-exp merge of the row's split partials, FP16
+// round-to-nearest output; thread d handles dim d of every head.  The
+// partials' (m, l) are fetched by parallel threads and every per-split load
+// is independent, so the merge costs a few memory round trips.
 __global__ void __launch_bounds__(kAttDim)
 attn_combine_kernel(const AttentionParams p) {
+  __shared__ float sm_m[kMaxSplits][kAttHeads], sm_l[kMaxSplits][kAttHeads];
+  __shared__ float w_s[kMaxSplits][kAttHeads];
+  __shared__ float inv_l[kAttHeads];
   const int r = blockIdx.x;
   const int d = threadIdx.x;
-  const float* base = p.part + (int64_t)r * p.nsplit * kPartFloats;
+  const int ns = p.nsplit;
+  const float* base = p.part + (int64_t)r * ns * kPartFloats;
+  if (d < ns * kAttHeads) {
+    const int s = d / kAttHeads, h = d % kAttHeads;
+    sm_m[s][h] = base[s * kPartFloats + h];
+    sm_l[s][h] = base[s * kPartFloats + kAttHeads + h];
+  }
+  // this thread's accumulators of every split, loaded up front
+  float a[kAttHeads][kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s)
+#pragma unroll
+    for (int h = 0; h < kAttHeads; ++h)
+      a[h][s] = s < ns ? base[s * kPartFloats + kAttHeads * 2 + h * kAttDim + d] : 0.f;
+  __syncthreads();
+  if (d < kAttHeads) {
+    const int h = d;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, sm_m[s][h]);
+    float L = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float w = M == -CUDART_INF_F ? 0.f : exp2f(sm_m[s][h] - M);
+      w_s[s][h] = w;
+      L = fmaf(w, sm_l[s][h], L);
+    }
+    inv_l[h] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
 #pragma unroll
   for (int h = 0; h < kAttHeads; ++h) {
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, base[s * kPartFloats + h]);
-    float o = 0.f;
-    if (M != -CUDART_INF_F) {
-      float A = 0.f, L = 0.f;
-      for (int s = 0; s < p.nsplit; ++s) {
-        const float* ps = base + s * kPartFloats;
-        const float c = exp2f(ps[h] - M);
-        A = fmaf(c, ps[kAttHeads * 2 + h * kAttDim + d], A);
-        L = fmaf(c, ps[kAttHeads + h], L);
-      }
-      o = A / L;
-    }
-    p.out[((int64_t)r * kAttHeads + h) * kAttDim + d] = __float2half_rn(o);
+    float A = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < ns) A = fmaf(w_s[s][h], a[h][s], A);
+    p.out[((int64_t)r * kAttHeads + h) * kAttDim + d] = __float2half_rn(A * inv_l[h]);
   }
 }
 

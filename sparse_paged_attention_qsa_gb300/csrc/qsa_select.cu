@@ -38,14 +38,18 @@ namespace {
 // score kernel: persistent, one CTA per SM, warp-specialised
 constexpr int kStages = 6;                              // 6 x 32 KiB pages in flight per SM
 constexpr int kPageBytes = kCmpPageKeys * kSelDim * 2;  // one compressed page
-constexpr int kScoreWarps = 8;                          // 16 keys of a page per warp
-constexpr int kScoreThreads = kScoreWarps * 32;
+#ifndef QSA_SCORE_WARPS
+#define QSA_SCORE_WARPS 8
+#endif
+constexpr int kScoreWarps = QSA_SCORE_WARPS;            // consumer warps: 8 or 16
+constexpr int kScoreThreads = (kScoreWarps + 1) * 32;   // + one producer warp
+constexpr int kScoreGroups = 16 / kScoreWarps;          // groups of 8 keys per warp per page
 constexpr int kMaxRows = 2048;                          // rows per launch (row tables in smem)
 constexpr size_t kScoreSmem = (size_t)kStages * kPageBytes + 1024 + 2 * kStages * 8 +
                               kStages * 16 + 3 * kMaxRows * sizeof(int);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s: any wait longer is a fault
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 512;                       // one key per thread in the sort
 
 struct RowSetup {
   int req;
@@ -198,15 +202,16 @@ struct StageDesc {
 // equal contiguous ranges, one per CTA (pages of one row are consecutive,
 // so a CTA changes rows rarely and reads consecutive page-table entries).
 //
-// Main loop: thread 0 walks its range and streams each page (32 KiB =
-// 128 keys x two 128-byte rows) into a ring of shared-memory stages with one
-// 2-D TMA load (128-byte swizzle, L2 evict-first), writing a small stage
-// descriptor (row, first block, key count) before arming the stage; it keeps
-// up to kStages pages in flight and blocks only for the stage this CTA is
-// about to consume.  All eight warps score 16 keys of each page.  With the
-// swizzle, lane (key k, slice t) reads row 2k + t/2, 16-byte chunks
-// (4(t&1)+j) XOR (row & 7): the 8 lanes of each shared-memory phase hit 8
-// distinct bank groups, and each lane reads its slice in ascending order.
+// Main loop, warp-specialised: lane 0 of the producer warp walks the CTA's
+// range and streams each page (32 KiB = 128 keys x two 128-byte rows) into a
+// ring of shared-memory stages with one 2-D TMA load (128-byte swizzle, L2
+// evict-first), writing a small stage descriptor (row, first block, key
+// count) before arming the stage; it refills a stage as soon as every
+// consumer warp has released it.  Each consumer warp scores 128/kScoreWarps
+// keys of every page.  With the swizzle, lane (key k, slice t) reads row
+// 2k + t/2, 16-byte chunks (4(t&1)+j) XOR (row & 7): the 8 lanes of each
+// shared-memory phase hit 8 distinct bank groups, and each lane reads its
+// slice in ascending order.
 __global__ void __launch_bounds__(kScoreThreads, 1)
 score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -226,9 +231,9 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const bool producer = tid == 0;
+  const bool is_producer_warp = warp == kScoreWarps;
 
-  if (producer) {
+  if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kScoreWarps);
@@ -238,97 +243,80 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
 
-  // ---- prologue: per-row visible pages and their prefix sum ----
-  constexpr int kRowsPerThread = kMaxRows / kScoreThreads;
-  int cnt[kRowsPerThread];
-  int mine = 0;
+  // ---- prologue (consumer threads): per-row visible pages, prefix sum ----
+  constexpr int kConsumerThreads = kScoreWarps * 32;
+  constexpr int kRowsPerThread = kMaxRows / kConsumerThreads;
+  if (!is_producer_warp) {
+    int cnt[kRowsPerThread];
+    int mine = 0;
 #pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) {
-    const int r = tid * kRowsPerThread + i;
-    cnt[i] = 0;
-    if (r < p.R) {
-      const RowSetup rs = row_setup(p, r);
-      const int64_t Vs = rs.ok ? (rs.V < p.vcap ? rs.V : p.vcap) : 0;
-      row_req[r] = rs.ok ? rs.req : -1;
-      row_vs[r] = (int)Vs;
-      cnt[i] = (int)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int r = tid * kRowsPerThread + i;
+      cnt[i] = 0;
+      if (r < p.R) {
+        const RowSetup rs = row_setup(p, r);
+        const int64_t Vs = rs.ok ? (rs.V < p.vcap ? rs.V : p.vcap) : 0;
+        row_req[r] = rs.ok ? rs.req : -1;
+        row_vs[r] = (int)Vs;
+        cnt[i] = (int)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
+      }
+      mine += cnt[i];
     }
-    mine += cnt[i];
-  }
-  int incl = mine;
+    int incl = mine;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sum[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  int64_t tot = 0;
-  for (int w = 0; w < kScoreWarps; ++w) {
-    before += (w < warp) ? warp_sum[w] : 0;
-    tot += warp_sum[w];
-  }
-  int run = before + incl - mine;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerThreads) : "memory");
+    int before = 0;
+    int64_t tot = 0;
+    for (int w = 0; w < kScoreWarps; ++w) {
+      before += (w < warp) ? warp_sum[w] : 0;
+      tot += warp_sum[w];
+    }
+    int run = before + incl - mine;
 #pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) {
-    const int r = tid * kRowsPerThread + i;
-    if (r < p.R) row_pre[r] = run;
-    run += cnt[i];
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int r = tid * kRowsPerThread + i;
+      if (r < p.R) row_pre[r] = run;
+      run += cnt[i];
+    }
+    if (tid == 0) s_total = tot;
   }
-  if (tid == 0) s_total = tot;
   __syncthreads();
 
   const int64_t W = s_total;
   const int64_t w_begin = W * blockIdx.x / gridDim.x;
   const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
   volatile int* abort_flag = &s_abort;
-
-  // producer state (thread 0 only)
   int64_t issued = 0;
-  int64_t pw = w_begin;
-  int prow = 0, pcol = 0;
-  bool ended = false;
-  uint64_t policy = 0;
-  if (producer) {
-    policy = evict_first_policy();
-    if (pw < w_end) {   // row holding page pw: last r with row_pre[r] <= pw and pages left
-      int lo = 0, hi = p.R - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (row_pre[mid] <= pw) lo = mid; else hi = mid - 1;
+
+  if (is_producer_warp) {
+    // ---------------- producer (one lane) ----------------
+    if (lane == 0) {
+      const uint64_t policy = evict_first_policy();
+      int64_t pw = w_begin;
+      int prow = 0, pcol = 0;
+      if (pw < w_end) {   // row holding page pw: last r with row_pre[r] <= pw
+        int lo = 0, hi = p.R - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (row_pre[mid] <= pw) lo = mid; else hi = mid - 1;
+        }
+        prow = lo;
+        pcol = (int)(pw - row_pre[prow]);
       }
-      prow = lo;
-      // rows with no pages share the prefix of the next row: step past them
-      while (row_pre[prow] + (int64_t)((row_vs[prow] + kCmpPageKeys - 1) / kCmpPageKeys) <= pw) ++prow;
-      pcol = (int)(pw - row_pre[prow]);
-    }
-  }
-
-  const int t = lane & 3;          // 32-dim slice of the key
-  const int kslot = lane >> 2;     // key within a group of 8
-  uint32_t q[kSelHeads][16];
-  int loaded_row = -1;
-  uint32_t* srow = nullptr;
-  int64_t used = 0;                // stages consumed
-
-  for (;;) {
-    // ---- keep the ring full (thread 0) ----
-    if (producer) {
-      while (!ended && issued < used + kStages && !*abort_flag) {
+      for (;;) {
         const int s = (int)(issued % kStages);
         const uint32_t ph = (uint32_t)((issued / kStages) & 1);
-        if (issued >= kStages) {
-          if (issued == used) {
-            if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
-              *abort_flag = 1;
-              report(p.err, kErrTimeout);
-              break;
-            }
-          } else if (!mbar_try_wait(bar_empty + 8 * s, ph ^ 1u)) {
-            break;
-          }
+        if (issued >= kStages && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeout);
+          break;
         }
+        if (*abort_flag) break;
         // next page with a loadable physical page (zero-fill the others)
         int32_t pg = -1;
         while (pw < w_end) {
@@ -355,6 +343,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
           report(p.err, kErrCmpPage);
           pg = -1;
         }
+        ++issued;
         if (pg >= 0) {
           mbar_expect_tx(bar_full + 8 * s, kPageBytes);
           tma_load_2d(base + s * kPageBytes, &tmap, 0, pg * 2 * kCmpPageKeys, bar_full + 8 * s,
@@ -362,66 +351,71 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
         } else {                    // range done: mark the stage as the end
           desc[s].row = -1;
           mbar_arrive(bar_full + 8 * s);
-          ended = true;
-        }
-        ++issued;
-      }
-    }
-    __syncwarp();
-    if (*abort_flag) break;
-
-    const int s = (int)(used % kStages);
-    const uint32_t ph = (uint32_t)((used / kStages) & 1);
-    if (!mbar_wait(bar_full + 8 * s, ph)) {
-      *abort_flag = 1;
-      report(p.err, kErrTimeout);
-      break;
-    }
-    const StageDesc d = desc[s];
-    if (d.row < 0) break;
-    if (d.row != loaded_row) {
-      loaded_row = d.row;
-      srow = p.scores + (int64_t)d.row * p.vcap;
-      // query slice [32t, 32t+32) of each head, fp16 pairs
-      const uint4* qp = reinterpret_cast<const uint4*>(p.q_sel + (int64_t)d.row * kSelHeads * kSelDim);
-#pragma unroll
-      for (int h = 0; h < kSelHeads; ++h) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = qp[h * 16 + t * 4 + i];
-          q[h][4 * i + 0] = v.x;
-          q[h][4 * i + 1] = v.y;
-          q[h][4 * i + 2] = v.z;
-          q[h][4 * i + 3] = v.w;
+          break;
         }
       }
     }
-    const uint32_t stage = base + s * kPageBytes;
-    uint4 kv[2][4];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const int k = warp * 16 + g * 8 + kslot;
-      const uint32_t row = 2 * k + (t >> 1);
-      const uint32_t rbase = stage + row * 128;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
-        kv[g][j] = lds128(rbase + chunk * 16);
+  } else {
+    // ---------------- consumers ----------------
+    const int t = lane & 3;          // 32-dim slice of the key
+    const int kslot = lane >> 2;     // key within a group of 8
+    uint32_t q[kSelHeads][16];
+    int loaded_row = -1;
+    uint32_t* srow = nullptr;
+    for (int64_t used = 0;; ++used) {
+      const int s = (int)(used % kStages);
+      const uint32_t ph = (uint32_t)((used / kStages) & 1);
+      if (!mbar_wait(bar_full + 8 * s, ph)) {
+        *abort_flag = 1;
+        report(p.err, kErrTimeout);
+        break;
       }
-    }
+      const StageDesc d = desc[s];
+      if (d.row < 0) break;
+      if (d.row != loaded_row) {
+        loaded_row = d.row;
+        srow = p.scores + (int64_t)d.row * p.vcap;
+        // query slice [32t, 32t+32) of each head, fp16 pairs
+        const uint4* qp = reinterpret_cast<const uint4*>(p.q_sel + (int64_t)d.row * kSelHeads * kSelDim);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const uint32_t key = quad_score(q, kv[g], t);
-      const int k = warp * 16 + g * 8 + kslot;
-      if (t == 0 && k < d.nkeys) srow[d.b0 + k] = key;
+        for (int h = 0; h < kSelHeads; ++h) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = qp[h * 16 + t * 4 + i];
+            q[h][4 * i + 0] = v.x;
+            q[h][4 * i + 1] = v.y;
+            q[h][4 * i + 2] = v.z;
+            q[h][4 * i + 3] = v.w;
+          }
+        }
+      }
+      const uint32_t stage = base + s * kPageBytes;
+      uint4 kv[kScoreGroups][4];
+#pragma unroll
+      for (int g = 0; g < kScoreGroups; ++g) {
+        const int k = (warp * kScoreGroups + g) * 8 + kslot;
+        const uint32_t row = 2 * k + (t >> 1);
+        const uint32_t rbase = stage + row * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
+          kv[g][j] = lds128(rbase + chunk * 16);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kScoreGroups; ++g) {
+        const uint32_t key = quad_score(q, kv[g], t);
+        const int k = (warp * kScoreGroups + g) * 8 + kslot;
+        if (t == 0 && k < d.nkeys) srow[d.b0 + k] = key;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
+      if (*abort_flag) break;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
-    ++used;
   }
   __syncthreads();
   // After a timeout, let every copy this CTA issued land before it exits.
-  if (*abort_flag && producer) {
+  if (*abort_flag && is_producer_warp && lane == 0) {
     const int64_t first = issued > kStages ? issued - kStages : 0;
     for (int64_t n = first; n < issued; ++n)
       mbar_wait(bar_full + 8 * (int)(n % kStages), (uint32_t)((n / kStages) & 1));
@@ -429,28 +423,139 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 }
 
 // ---------------------------------------------------------------------------
-// top-k: exact radix select over 32-bit ordered score keys
+// top-k: exact selection of the row's 512 largest 32-bit ordered score keys
 // ---------------------------------------------------------------------------
+//
+// One CTA per row.  Keys are bits(score)+1 (bit 31 clear, 0 = no key).
+//  1. One sweep counts the keys and takes each thread's maximum.  If at least
+//     K = min(512, #keys) threads hold a key, the smallest of those maxima is
+//     a lower bound L0 of the K-th largest key (at least K distinct keys --
+//     the maxima -- are >= it); otherwise L0 = 1.
+//  2. A second sweep appends every key >= L0 (with its block index) to a
+//     candidate list in shared memory: about 9 % of a 32768-key row.
+//  3. MSB-first radix select over the candidates (digits 30..20, 19..9,
+//     8..0) finds T, the K-th largest key, and `need`, how many keys equal
+//     to T belong to the top K.  If more than `need` keys equal T, a second
+//     radix select over (2^31-1 - block index) of those ties keeps the
+//     `need` smallest block indices (the tie rule).
+//  4. The K (key, ~index) pairs are bitonic-sorted, expanded, tail appended.
+// A row whose candidates overflow the list falls back to radix passes over
+// all of its keys, re-read from the workspace (L2).
 
-__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t bin, int lane) {
-  const unsigned m = __match_any_sync(0xffffffffu, bin);
-  if (bin < 256u && lane == __ffs(m) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(m));
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kCandCap = 8192;
+constexpr int kSweepUnroll = 8;
+
+struct TopkShared {
+  uint32_t hist[2048];
+  unsigned long long keys[kTopkBlocks];
+  uint32_t cand_x[kCandCap];
+  uint32_t cand_i[kCandCap];
+  uint32_t wsum[kTopkWarps];
+  uint32_t wmin[kTopkWarps];
+  uint32_t wcnt[kTopkWarps];
+  uint32_t found_digit, found_above;
+  int count, ncand;
+};
+constexpr size_t kTopkSmem = sizeof(TopkShared);
+
+// Suffix scan of the histogram: find the digit d with
+// above(d) < need <= above(d) + hist[d]; returns d and above(d).
+__device__ __forceinline__ void find_digit(TopkShared& sh, int nbins, uint32_t need, int tid,
+                                           int lane, int warp) {
+  const int per = nbins / kTopkThreads;          // 4 or 1 bins per thread
+  uint32_t local = 0;
+  for (int b = 0; b < per; ++b) local += sh.hist[tid * per + b];
+  uint32_t suf = local;                           // inclusive suffix within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  if (lane == 0) sh.wsum[warp] = suf;
+  __syncthreads();
+  uint32_t higher = 0;
+  for (int w = warp + 1; w < kTopkWarps; ++w) higher += sh.wsum[w];
+  uint32_t above = higher + suf - local;          // keys in bins above this thread's
+  if (need > 0 && above < need && above + local >= need) {
+    for (int b = per - 1; b >= 0; --b) {
+      const uint32_t h = sh.hist[tid * per + b];
+      if (above + h >= need) {
+        sh.found_digit = (uint32_t)(tid * per + b);
+        sh.found_above = above;
+        break;
+      }
+      above += h;
+    }
+  }
+  __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// Radix select over n items: item_key gives item c's key (< 2^31; 0 = not a
+// member).  Returns T, the k-th largest member key, `need` (how many members
+// equal to T are in the top k) and the number of members equal to T.
+struct Selected {
+  uint32_t T, need, eq_total;
+};
+
+// item keys for radix_select: the candidate list or all of the row's keys,
+// either as is or as (2^31-1 - block index) of the ties equal to T
+enum KeyMode { kCand = 0, kCandTie = 1, kRow = 2, kRowTie = 3 };
+
+template <int Mode>
+__device__ __forceinline__ uint32_t item_key(const TopkShared& sh, const uint32_t* sc, int64_t c,
+                                             uint32_t T) {
+  if (Mode == kCand) return sh.cand_x[c];
+  if (Mode == kCandTie) return sh.cand_x[c] == T ? 0x7fffffffu - sh.cand_i[c] : 0u;
+  if (Mode == kRow) return sc[c];
+  return sc[c] == T ? 0x7fffffffu - (uint32_t)c : 0u;
+}
+
+template <int Mode>
+__device__ __forceinline__ Selected radix_select(TopkShared& sh, const uint32_t* sc, int64_t n,
+                                                 uint32_t k, uint32_t T = 0) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, pmask = 0, need = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 20 : (pass == 1 ? 9 : 0);   // digits 30..20, 19..9, 8..0
+    const int nbins = pass == 2 ? 512 : 2048;
+    const uint32_t dmask = (uint32_t)nbins - 1u;
+    for (int i = tid; i < nbins; i += kTopkThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int64_t c = tid; c < n; c += kTopkThreads) {
+      const uint32_t x = item_key<Mode>(sh, sc, c, T);
+      if (x != 0u && (x & pmask) == prefix) atomicAdd(&sh.hist[(x >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    find_digit(sh, nbins, need, tid, lane, warp);
+    prefix |= sh.found_digit << shift;
+    pmask |= dmask << shift;
+    need -= sh.found_above;
+    __syncthreads();
+  }
+  Selected r{prefix, need, sh.hist[prefix & 511u]};   // last pass: one bin per key value
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void emit_key(TopkShared& sh, uint32_t x, int64_t idx) {
+  const int slot = atomicAdd(&sh.count, 1);
+  sh.keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2)
 topk_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) unsigned char topk_smem[];
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   const int r = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  constexpr int kWarps = kTopkThreads / 32;
-
-  __shared__ uint32_t hist[256];
-  __shared__ unsigned long long keys[kTopkBlocks];
-  __shared__ uint32_t warp_cnt[kWarps];
-  __shared__ uint32_t s_prefix, s_krem, s_nvalid;
-  __shared__ int s_count;
-
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RowSetup rs = row_setup(p, r);
   int32_t* out = p.out + (int64_t)r * p.out_stride0;
   if (!rs.ok) {
@@ -462,108 +567,128 @@ topk_kernel(const SelectParams p) {
   const int64_t Vs = rs.V < p.vcap ? rs.V : p.vcap;
   const uint32_t* sc = p.scores + (int64_t)r * p.vcap;
 
-  uint32_t prefix = 0, pmask = 0, K = 0, krem = 0;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    for (int64_t base = 0; base < Vs; base += kTopkThreads) {
-      const int64_t i = base + tid;
-      const uint32_t x = i < Vs ? sc[i] : 0u;
-      const bool match = x != 0u && (x & pmask) == prefix;
-      warp_hist_add(hist, match ? (x >> shift) & 255u : 256u, lane);
+  // 1. count keys, per-thread maxima, lower bound L0 (8 loads in flight)
+  uint32_t tmax = 0, cnt = 0;
+  for (int64_t base = tid; base < Vs; base += kTopkThreads * kSweepUnroll) {
+    uint32_t x[kSweepUnroll];
+#pragma unroll
+    for (int u = 0; u < kSweepUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kTopkThreads;
+      x[u] = i < Vs ? sc[i] : 0u;
     }
-    __syncthreads();
-    if (tid == 0) {
-      if (pass == 0) {
-        uint32_t n = 0;
-        for (int d = 0; d < 256; ++d) n += hist[d];
-        s_nvalid = n;
-        s_krem = n < (uint32_t)kTopkBlocks ? n : (uint32_t)kTopkBlocks;
-      }
-      uint32_t need = s_krem, above = 0;
-      int dsel = 0;
-      if (need > 0) {
-        for (int d = 255; d >= 0; --d) {
-          if (above + hist[d] >= need) { dsel = d; break; }
-          above += hist[d];
-        }
-      }
-      s_krem = need - above;
-      s_prefix = prefix | ((uint32_t)dsel << shift);
+#pragma unroll
+    for (int u = 0; u < kSweepUnroll; ++u) {
+      tmax = x[u] > tmax ? x[u] : tmax;
+      cnt += x[u] != 0u;
     }
-    __syncthreads();
-    if (pass == 0) K = s_nvalid < (uint32_t)kTopkBlocks ? s_nvalid : (uint32_t)kTopkBlocks;
-    if (K == 0) break;
-    prefix = s_prefix;
-    pmask |= 255u << shift;
-    krem = s_krem;
+  }
+  {
+    uint32_t mn = tmax != 0u ? tmax : 0xffffffffu;
+    uint32_t ne = tmax != 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      ne += __shfl_xor_sync(0xffffffffu, ne, o);
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) { sh.wsum[warp] = cnt; sh.wcnt[warp] = ne; sh.wmin[warp] = mn; }
+    if (tid == 0) { sh.count = 0; sh.ncand = 0; }
     __syncthreads();
   }
-
-  if (K > 0) {
-    const uint32_t T = prefix;   // the K-th largest key value
-    if (tid == 0) s_count = 0;
-    __syncthreads();
-    // every key strictly above T is in
-    for (int64_t i = tid; i < Vs; i += kTopkThreads) {
-      const uint32_t x = sc[i];
-      if (x > T) {
-        const int slot = atomicAdd(&s_count, 1);
-        keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)i);
-      }
-    }
-    // among keys equal to T, the krem with the smallest block index
-    uint32_t taken = 0;
-    for (int64_t base = 0; base < Vs && taken < krem; base += kTopkThreads) {
-      const int64_t i = base + tid;
-      const bool eq = i < Vs && sc[i] == T;
-      const unsigned bal = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) warp_cnt[warp] = __popc(bal);
-      __syncthreads();
-      uint32_t off = 0, tot = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        const uint32_t c = warp_cnt[w];
-        off += (w < warp) ? c : 0u;
-        tot += c;
-      }
-      const uint32_t rank = taken + off + __popc(bal & ((1u << lane) - 1u));
-      if (eq && rank < krem) {
-        const int slot = atomicAdd(&s_count, 1);
-        keys[slot] = ((unsigned long long)T << 32) | (0xffffffffu - (uint32_t)i);
-      }
-      taken += tot;
-      __syncthreads();
-    }
-    __syncthreads();
+  uint32_t nkeys = 0, nonempty = 0, minmax = 0xffffffffu;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    nkeys += sh.wsum[w];
+    nonempty += sh.wcnt[w];
+    minmax = min(minmax, sh.wmin[w]);
   }
-  for (int i = (int)K + tid; i < kTopkBlocks; i += kTopkThreads) keys[i] = 0ull;
+  const uint32_t K = nkeys < (uint32_t)kTopkBlocks ? nkeys : (uint32_t)kTopkBlocks;
   __syncthreads();
 
-  // bitonic sort, descending (score desc, then block asc via the ~index)
-  for (int k = 2; k <= kTopkBlocks; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < kTopkBlocks; i += kTopkThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = keys[i], c = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < c) : (a > c)) { keys[i] = c; keys[ixj] = a; }
+  if (K > 0) {
+    const uint32_t L0 = nonempty >= K ? minmax : 1u;
+    // 2. candidates >= L0, appended warp by warp (8 loads in flight)
+    for (int64_t base = 0; base < Vs; base += kTopkThreads * kSweepUnroll) {
+      uint32_t x[kSweepUnroll];
+#pragma unroll
+      for (int u = 0; u < kSweepUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
+        x[u] = i < Vs ? sc[i] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kSweepUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
+        const bool take = x[u] != 0u && x[u] >= L0;
+        const unsigned bal = __ballot_sync(0xffffffffu, take);
+        int wbase = 0;
+        if (lane == 0 && bal) wbase = atomicAdd(&sh.ncand, __popc(bal));
+        wbase = __shfl_sync(0xffffffffu, wbase, 0);
+        if (take) {
+          const int slot = wbase + __popc(bal & ((1u << lane) - 1u));
+          if (slot < kCandCap) { sh.cand_x[slot] = x[u]; sh.cand_i[slot] = (uint32_t)i; }
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
+    const int n = sh.ncand;
+    if (n <= kCandCap) {
+      // 3. radix select over the candidates
+      const Selected sel = radix_select<kCand>(sh, sc, n, K);
+      const uint32_t T = sel.T;
+      const bool all_eq = sel.eq_total == sel.need;
+      for (int c = tid; c < n; c += kTopkThreads) {
+        const uint32_t x = sh.cand_x[c];
+        if (x > T || (x == T && all_eq)) emit_key(sh, x, sh.cand_i[c]);
+      }
+      if (!all_eq) {   // surplus ties at T: keep the smallest block indices
+        const Selected si = radix_select<kCandTie>(sh, sc, n, sel.need, T);
+        for (int c = tid; c < n; c += kTopkThreads)
+          if (sh.cand_x[c] == T && 0x7fffffffu - sh.cand_i[c] >= si.T) emit_key(sh, T, sh.cand_i[c]);
+      }
+    } else {
+      // fallback: radix select over all keys of the row (from the workspace)
+      const Selected sel = radix_select<kRow>(sh, sc, Vs, K);
+      const uint32_t T = sel.T;
+      const bool all_eq = sel.eq_total == sel.need;
+      for (int64_t i = tid; i < Vs; i += kTopkThreads) {
+        const uint32_t x = sc[i];
+        if (x > T || (x == T && all_eq)) emit_key(sh, x, i);
+      }
+      if (!all_eq) {
+        const Selected si = radix_select<kRowTie>(sh, sc, Vs, sel.need, T);
+        for (int64_t i = tid; i < Vs; i += kTopkThreads)
+          if (sc[i] == T && 0x7fffffffu - (uint32_t)i >= si.T) emit_key(sh, T, i);
+      }
+    }
+    __syncthreads();
   }
 
-  // expand kept blocks, then tail, then -1
-  for (int j = tid; j < (int)K; j += kTopkThreads) {
-    const int32_t b = (int32_t)(0xffffffffu - (uint32_t)(keys[j] & 0xffffffffull));
+  // 4. bitonic sort, descending: key first, then ascending block (via ~index)
+  unsigned long long a = tid < (int)K ? sh.keys[tid] : 0ull;
+  for (int k = 2; k <= kTopkBlocks; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long b;
+      if (j < 32) {
+        b = shfl_xor_u64(a, j);
+      } else {
+        __syncthreads();
+        sh.keys[tid] = a;
+        __syncthreads();
+        b = sh.keys[tid ^ j];
+      }
+      const bool desc = (tid & k) == 0;
+      const bool lower = (tid & j) == 0;
+      const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+      a = (desc == lower) ? hi : lo;
+    }
+  }
+  // expand kept blocks, then the tail, then -1
+  if (tid < (int)K) {
+    const int32_t b = (int32_t)(0xffffffffu - (uint32_t)(a & 0xffffffffull));
     const int32_t tok = b * kRatio;
-    out[4 * j + 0] = tok;
-    out[4 * j + 1] = tok + 1;
-    out[4 * j + 2] = tok + 2;
-    out[4 * j + 3] = tok + 3;
+    out[4 * tid + 0] = tok;
+    out[4 * tid + 1] = tok + 1;
+    out[4 * tid + 2] = tok + 2;
+    out[4 * tid + 3] = tok + 3;
   }
   const int64_t tail0 = rs.V * kRatio;
   const int64_t tail_len = rs.tail_end >= tail0 ? rs.tail_end - tail0 + 1 : 0;
@@ -633,6 +758,9 @@ cudaError_t device_info(DeviceInfo** out) {
     e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScoreSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
     d.smem_set = true;
   }
   *out = &d;
@@ -661,7 +789,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
     score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
-    topk_kernel<<<c.R, kTopkThreads, 0, stream>>>(c);
+    topk_kernel<<<c.R, kTopkThreads, kTopkSmem, stream>>>(c);
   }
   return cudaGetLastError();
 }
