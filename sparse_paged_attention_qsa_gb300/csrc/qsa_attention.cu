@@ -91,6 +91,7 @@ attn_partial_kernel(const AttentionParams p) {
   __shared__ float sm_acc[kAttWarps][kAttHeads][kAttDim];
   __shared__ uint32_t sm_tok[kAttWarps][32];
 
+  pdl_trigger();   // the combine kernel may be scheduled early (it waits)
   const int req = p.t2r[r];
   const bool rok = req >= 0 && req < p.num_reqs;
   if (!rok && split == 0 && tid == 0) report(p.err, kErrRequest);
@@ -256,6 +257,7 @@ attn_combine_kernel(const AttentionParams p) {
   const int d = threadIdx.x;
   const int ns = p.nsplit;
   const float* base = p.part + (int64_t)r * ns * kPartFloats;
+  pdl_wait();      // every split partial is written and visible
   if (d < ns * kAttHeads) {
     const int s = d / kAttHeads, h = d % kAttHeads;
     sm_m[s][h] = base[s * kPartFloats + h];
@@ -308,8 +310,9 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
   dim3 grid((unsigned)p.nsplit, (unsigned)p.R);
   attn_partial_kernel<<<grid, kAttThreads, 0, stream>>>(p);
-  attn_combine_kernel<<<p.R, kAttDim, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_after(attn_combine_kernel, dim3(p.R), dim3(kAttDim), 0, stream, p);
 }
 
 }  // namespace qsa

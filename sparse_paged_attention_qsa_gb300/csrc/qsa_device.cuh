@@ -35,6 +35,14 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor finishes; pdl_wait() blocks
+// until the predecessor grid has completed and its writes are visible (a
+// no-op without the launch attribute).  pdl_trigger() lets the successor be
+// scheduled once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void report(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -65,6 +66,25 @@ struct AttentionParams {
   uint32_t* err;              // nullable
   int R;
 };
+
+// Launch `kernel` so that it may start while the previous kernel in the
+// stream is finishing (programmatic dependent launch); the kernel must call
+// pdl_wait() before reading what that kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 size_t select_workspace_bytes(int64_t R, int64_t pt_cols);
 size_t attention_workspace_bytes(int64_t R, int64_t width);

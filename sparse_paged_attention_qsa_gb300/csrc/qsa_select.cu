@@ -232,6 +232,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool is_producer_warp = warp == kScoreWarps;
+  pdl_trigger();   // the top-k kernel may be scheduled wherever a CTA has exited
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -438,12 +439,14 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 //     to T belong to the top K.  If more than `need` keys equal T, a second
 //     radix select over (2^31-1 - block index) of those ties keeps the
 //     `need` smallest block indices (the tie rule).
-//  4. The K (key, ~index) pairs are bitonic-sorted, expanded, tail appended.
+//  4. The K (key, ~index) pairs are ordered (warp sorts + rank merge),
+//     expanded, tail appended.
 // A row whose candidates overflow the list falls back to radix passes over
 // all of its keys, re-read from the workspace (L2).
 
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 8192;
+constexpr int kWarpCand = kCandCap / kTopkWarps;        // 512 slots per warp region
 constexpr int kSweepUnroll = 8;
 
 struct TopkShared {
@@ -454,8 +457,9 @@ struct TopkShared {
   uint32_t wsum[kTopkWarps];
   uint32_t wmin[kTopkWarps];
   uint32_t wcnt[kTopkWarps];
+  uint32_t wcand[kTopkWarps];      // candidates in each warp's region
   uint32_t found_digit, found_above;
-  int count, ncand;
+  int count;
 };
 constexpr size_t kTopkSmem = sizeof(TopkShared);
 
@@ -505,8 +509,11 @@ enum KeyMode { kCand = 0, kCandTie = 1, kRow = 2, kRowTie = 3 };
 template <int Mode>
 __device__ __forceinline__ uint32_t item_key(const TopkShared& sh, const uint32_t* sc, int64_t c,
                                              uint32_t T) {
-  if (Mode == kCand) return sh.cand_x[c];
-  if (Mode == kCandTie) return sh.cand_x[c] == T ? 0x7fffffffu - sh.cand_i[c] : 0u;
+  if (Mode == kCand || Mode == kCandTie) {
+    if ((uint32_t)(c % kWarpCand) >= sh.wcand[c / kWarpCand]) return 0u;   // empty slot
+    if (Mode == kCand) return sh.cand_x[c];
+    return sh.cand_x[c] == T ? 0x7fffffffu - sh.cand_i[c] : 0u;
+  }
   if (Mode == kRow) return sc[c];
   return sc[c] == T ? 0x7fffffffu - (uint32_t)c : 0u;
 }
@@ -539,9 +546,18 @@ __device__ __forceinline__ Selected radix_select(TopkShared& sh, const uint32_t*
   return r;
 }
 
-__device__ __forceinline__ void emit_key(TopkShared& sh, uint32_t x, int64_t idx) {
-  const int slot = atomicAdd(&sh.count, 1);
-  sh.keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
+// Append (key, ~index) for the lanes with `take`; one shared atomic per warp.
+// Every lane of the warp must call this together.
+__device__ __forceinline__ void emit_warp(TopkShared& sh, bool take, uint32_t x, int64_t idx,
+                                          int lane) {
+  const unsigned bal = __ballot_sync(0xffffffffu, take);
+  if (!bal) return;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(&sh.count, __popc(bal));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (take)
+    sh.keys[base + __popc(bal & ((1u << lane) - 1u))] =
+        ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
 }
 
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
@@ -559,6 +575,7 @@ topk_kernel(const SelectParams p) {
   const RowSetup rs = row_setup(p, r);
   int32_t* out = p.out + (int64_t)r * p.out_stride0;
   if (!rs.ok) {
+    pdl_wait();
     for (int j = tid; j < kOutWidth; j += kTopkThreads) out[j] = -1;
     if (tid == 0) report(p.err, kErrRequest);
     return;
@@ -566,6 +583,7 @@ topk_kernel(const SelectParams p) {
   if (tid == 0 && rs.V > p.vcap) report(p.err, kErrCmpPage);
   const int64_t Vs = rs.V < p.vcap ? rs.V : p.vcap;
   const uint32_t* sc = p.scores + (int64_t)r * p.vcap;
+  pdl_wait();      // the score kernel's keys are complete and visible
 
   // 1. count keys, per-thread maxima, lower bound L0 (8 loads in flight)
   uint32_t tmax = 0, cnt = 0;
@@ -592,7 +610,7 @@ topk_kernel(const SelectParams p) {
       mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     }
     if (lane == 0) { sh.wsum[warp] = cnt; sh.wcnt[warp] = ne; sh.wmin[warp] = mn; }
-    if (tid == 0) { sh.count = 0; sh.ncand = 0; }
+    if (tid == 0) sh.count = 0;
     __syncthreads();
   }
   uint32_t nkeys = 0, nonempty = 0, minmax = 0xffffffffu;
@@ -606,7 +624,11 @@ topk_kernel(const SelectParams p) {
 
   if (K > 0) {
     const uint32_t L0 = nonempty >= K ? minmax : 1u;
-    // 2. candidates >= L0, appended warp by warp (8 loads in flight)
+    // 2. candidates >= L0 into this warp's region (a register counter per
+    // warp, no atomics; 8 loads in flight)
+    uint32_t wcount = 0;
+    uint32_t* cx = sh.cand_x + warp * kWarpCand;
+    uint32_t* ci = sh.cand_i + warp * kWarpCand;
     for (int64_t base = 0; base < Vs; base += kTopkThreads * kSweepUnroll) {
       uint32_t x[kSweepUnroll];
 #pragma unroll
@@ -616,80 +638,104 @@ topk_kernel(const SelectParams p) {
       }
 #pragma unroll
       for (int u = 0; u < kSweepUnroll; ++u) {
-        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
         const bool take = x[u] != 0u && x[u] >= L0;
         const unsigned bal = __ballot_sync(0xffffffffu, take);
-        int wbase = 0;
-        if (lane == 0 && bal) wbase = atomicAdd(&sh.ncand, __popc(bal));
-        wbase = __shfl_sync(0xffffffffu, wbase, 0);
-        if (take) {
-          const int slot = wbase + __popc(bal & ((1u << lane) - 1u));
-          if (slot < kCandCap) { sh.cand_x[slot] = x[u]; sh.cand_i[slot] = (uint32_t)i; }
+        const uint32_t pos = wcount + __popc(bal & ((1u << lane) - 1u));
+        if (take && pos < (uint32_t)kWarpCand) {
+          cx[pos] = x[u];
+          ci[pos] = (uint32_t)(base + (int64_t)u * kTopkThreads + tid);
         }
+        wcount += __popc(bal);
       }
     }
+    if (lane == 0) sh.wcand[warp] = wcount;
     __syncthreads();
-    const int n = sh.ncand;
-    if (n <= kCandCap) {
-      // 3. radix select over the candidates
-      const Selected sel = radix_select<kCand>(sh, sc, n, K);
+    bool fits = true;
+    for (int w = 0; w < kTopkWarps; ++w) fits &= sh.wcand[w] <= (uint32_t)kWarpCand;
+    if (fits) {
+      // 3. radix select over the candidate regions
+      const Selected sel = radix_select<kCand>(sh, sc, kCandCap, K);
       const uint32_t T = sel.T;
       const bool all_eq = sel.eq_total == sel.need;
-      for (int c = tid; c < n; c += kTopkThreads) {
-        const uint32_t x = sh.cand_x[c];
-        if (x > T || (x == T && all_eq)) emit_key(sh, x, sh.cand_i[c]);
+      // each warp emits from its own region
+      for (uint32_t c = lane; c < ((wcount + 31u) & ~31u); c += 32) {
+        const bool in = c < wcount;
+        const uint32_t x = in ? cx[c] : 0u;
+        emit_warp(sh, in && (x > T || (x == T && all_eq)), x, in ? ci[c] : 0u, lane);
       }
       if (!all_eq) {   // surplus ties at T: keep the smallest block indices
-        const Selected si = radix_select<kCandTie>(sh, sc, n, sel.need, T);
-        for (int c = tid; c < n; c += kTopkThreads)
-          if (sh.cand_x[c] == T && 0x7fffffffu - sh.cand_i[c] >= si.T) emit_key(sh, T, sh.cand_i[c]);
+        const Selected si = radix_select<kCandTie>(sh, sc, kCandCap, sel.need, T);
+        for (uint32_t c = lane; c < ((wcount + 31u) & ~31u); c += 32) {
+          const bool in = c < wcount;
+          const bool take = in && cx[c] == T && 0x7fffffffu - ci[c] >= si.T;
+          emit_warp(sh, take, T, in ? ci[c] : 0u, lane);
+        }
       }
     } else {
       // fallback: radix select over all keys of the row (from the workspace)
       const Selected sel = radix_select<kRow>(sh, sc, Vs, K);
       const uint32_t T = sel.T;
       const bool all_eq = sel.eq_total == sel.need;
-      for (int64_t i = tid; i < Vs; i += kTopkThreads) {
-        const uint32_t x = sc[i];
-        if (x > T || (x == T && all_eq)) emit_key(sh, x, i);
+      for (int64_t b0 = 0; b0 < Vs; b0 += kTopkThreads) {
+        const int64_t i = b0 + tid;
+        const uint32_t x = i < Vs ? sc[i] : 0u;
+        emit_warp(sh, x != 0u && (x > T || (x == T && all_eq)), x, i, lane);
       }
       if (!all_eq) {
         const Selected si = radix_select<kRowTie>(sh, sc, Vs, sel.need, T);
-        for (int64_t i = tid; i < Vs; i += kTopkThreads)
-          if (sc[i] == T && 0x7fffffffu - (uint32_t)i >= si.T) emit_key(sh, T, i);
+        for (int64_t b0 = 0; b0 < Vs; b0 += kTopkThreads) {
+          const int64_t i = b0 + tid;
+          const bool take = i < Vs && sc[i] == T && 0x7fffffffu - (uint32_t)i >= si.T;
+          emit_warp(sh, take, T, i, lane);
+        }
       }
     }
     __syncthreads();
   }
 
-  // 4. bitonic sort, descending: key first, then ascending block (via ~index)
+  // 4. order: each warp sorts its 32 keys descending with shuffles; a key's
+  // final position is its place in its warp's list plus, for every other
+  // warp's list, how many keys there are larger (binary search).  Kept keys
+  // are distinct and nonzero, so their positions are exactly 0..K-1.
   unsigned long long a = tid < (int)K ? sh.keys[tid] : 0ull;
-  for (int k = 2; k <= kTopkBlocks; k <<= 1) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      unsigned long long b;
-      if (j < 32) {
-        b = shfl_xor_u64(a, j);
-      } else {
-        __syncthreads();
-        sh.keys[tid] = a;
-        __syncthreads();
-        b = sh.keys[tid ^ j];
-      }
-      const bool desc = (tid & k) == 0;
-      const bool lower = (tid & j) == 0;
+      const unsigned long long b = shfl_xor_u64(a, j);
+      const bool desc = (lane & k) == 0 || k == 32;
+      const bool lower = (lane & j) == 0;
       const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
       a = (desc == lower) ? hi : lo;
     }
   }
-  // expand kept blocks, then the tail, then -1
-  if (tid < (int)K) {
+  __syncthreads();
+  sh.keys[tid] = a;
+  __syncthreads();
+  if (a != 0ull) {
+    int rank = lane;
+    for (int w = 0; w < kTopkWarps; ++w) {
+      if (w == warp) continue;
+      const unsigned long long* lst = sh.keys + w * 32;
+      int pos = 0;                                   // keys in lst larger than a
+      if (lst[31] > a) {
+        pos = 32;
+      } else {
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1)
+          if (lst[pos + step - 1] > a) pos += step;
+      }
+      rank += pos;
+    }
+    // expand the kept block at its position
     const int32_t b = (int32_t)(0xffffffffu - (uint32_t)(a & 0xffffffffull));
     const int32_t tok = b * kRatio;
-    out[4 * tid + 0] = tok;
-    out[4 * tid + 1] = tok + 1;
-    out[4 * tid + 2] = tok + 2;
-    out[4 * tid + 3] = tok + 3;
+    out[4 * rank + 0] = tok;
+    out[4 * rank + 1] = tok + 1;
+    out[4 * rank + 2] = tok + 2;
+    out[4 * rank + 3] = tok + 3;
   }
+  // then the tail, then -1
   const int64_t tail0 = rs.V * kRatio;
   const int64_t tail_len = rs.tail_end >= tail0 ? rs.tail_end - tail0 + 1 : 0;
   for (int j = 4 * (int)K + tid; j < kOutWidth; j += kTopkThreads) {
@@ -789,7 +835,8 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
     score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
-    topk_kernel<<<c.R, kTopkThreads, kTopkSmem, stream>>>(c);
+    e = launch_after(topk_kernel, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
