@@ -42,6 +42,29 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic_R256_L131072.json")
+
+
+def _selection_traffic(workload: int, rows: int):
+    """DRAM bytes per selection launch from the committed ncu summary, or
+    None when the kernels changed since the capture (source hashes differ)
+    or the workload is not the one captured."""
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        if workload != 4 or rows != d["rows_scaled_to"]:
+            return None
+        csrc = os.path.join(ROOT, "sparse_paged_attention_qsa_gb300", "csrc")
+        for name, digest in d["sources_sha256"].items():
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        return int(d["selection_stage_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -392,7 +415,8 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "selection stage (score + top-k launches)",
                      "achieved": sel_gbs, "peak": peak, "unit": "GB/s",
                      "frac": sel_gbs / peak, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": sel_bytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": sel_bytes,
+                     "traffic": _selection_traffic(args.workload, R)},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms, "steps": Ke},
