@@ -69,6 +69,13 @@ def _load():
         i64, u32, vp = ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
         lib.qsa_oracle_half_to_double.restype = ctypes.c_double
         lib.qsa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.qsa_oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.qsa_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.qsa_oracle_score_e4m3.restype = ctypes.c_float
+        lib.qsa_oracle_score_e4m3.argtypes = [vp, vp]
+        lib.qsa_oracle_select_keys.restype = u32
+        lib.qsa_oracle_select_keys.argtypes = [i64, vp, ctypes.c_int, vp, i64, vp, i64, i64, i64,
+                                               vp, vp, vp, vp, i64]
         lib.qsa_oracle_score.restype = ctypes.c_float
         lib.qsa_oracle_score.argtypes = [vp, vp]
         lib.qsa_oracle_visible_blocks.restype = i64
@@ -97,6 +104,17 @@ def _u16(a) -> np.ndarray:
     return np.ascontiguousarray(a)
 
 
+def _u8(a) -> np.ndarray:
+    """E4M3 bytes (uint8, or any 1-byte dtype) -> C-contiguous uint8."""
+    a = np.asarray(a)
+    if a.dtype.itemsize != 1:
+        raise TypeError(f"expected 1-byte elements, got {a.dtype}")
+    return np.ascontiguousarray(a.view(np.uint8))
+
+
+KEY_F16, KEY_E4M3 = 0, 1
+
+
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
@@ -106,24 +124,30 @@ class PagePool:
 
     ``pages`` is either a contiguous array whose first axis is the page id, or
     a dict {page_id: page array} for a pool of ``num_pages`` where only some
-    pages are present (the rest read as absent).  Pages are kept alive here.
+    pages are present (the rest read as absent).  ``kind`` is KEY_F16 (fp16
+    elements, also used for K/V pages) or KEY_E4M3 (one byte per element).
+    Pages are kept alive here.
     """
 
-    def __init__(self, pages, num_pages: int | None = None, page_halves: int = 0):
+    def __init__(self, pages, num_pages: int | None = None, page_halves: int = 0,
+                 kind: int = KEY_F16):
         self._keep = []
+        self.kind = kind
+        conv = _u8 if kind == KEY_E4M3 else _u16
+        esize = 1 if kind == KEY_E4M3 else 2
         if isinstance(pages, dict):
             if num_pages is None:
                 raise ValueError("num_pages is required for a sparse pool")
             self.num_pages = int(num_pages)
             arr = (ctypes.c_void_p * max(self.num_pages, 1))()
             for pid, pg in pages.items():
-                pg = _u16(pg)
+                pg = conv(pg)
                 if page_halves and pg.size != page_halves:
                     raise ValueError("page of wrong size")
                 self._keep.append(pg)
                 arr[int(pid)] = _ptr(pg)
         else:
-            pool = _u16(pages)
+            pool = conv(pages)
             self.num_pages = int(pool.shape[0]) if num_pages is None else int(num_pages)
             self._keep.append(pool)
             arr = (ctypes.c_void_p * max(self.num_pages, 1))()
@@ -133,12 +157,23 @@ class PagePool:
                     raise ValueError("page of wrong size")
                 base = _ptr(pool)
                 for p in range(min(self.num_pages, pool.shape[0])):
-                    arr[p] = base + 2 * per * p
+                    arr[p] = base + esize * per * p
         self.array = arr
 
 
 def half_to_double(bits: int) -> float:
     return _load().qsa_oracle_half_to_double(int(bits) & 0xFFFF)
+
+
+def e4m3_to_double(bits: int) -> float:
+    return _load().qsa_oracle_e4m3_to_double(int(bits) & 0xFF)
+
+
+def score_e4m3(q_sel_row, key_bytes) -> np.float32:
+    """Canonical binary32 score of one E4M3 key [128 bytes] against q [4,128]."""
+    q = _u16(q_sel_row).reshape(4, 128)
+    k = _u8(key_bytes).reshape(128)
+    return np.float32(_load().qsa_oracle_score_e4m3(_ptr(q), _ptr(k)))
 
 
 def score(q_sel_row, key) -> np.float32:
@@ -167,12 +202,18 @@ def select(q_sel, cmp_pool, cmp_page_table, token_to_request, seq_lens,
            threads: int = 1):
     """Selection for all rows; returns (indices [R,out_width] int32, err bits
     [, scores [R,512] float32]).  ``cmp_pool`` is a PagePool or an array
-    [P,128,1,128] fp16.  Rows are independent; ``threads`` splits them over
+    [P,128,1,128] of fp16 keys or of E4M3 key bytes (any 1-byte dtype).  Rows are independent; ``threads`` splits them over
     OS threads (the C code itself is single-threaded)."""
     lib = _load()
     q = _u16(q_sel).reshape(-1, 4, 128)
     R = q.shape[0]
-    pool = cmp_pool if isinstance(cmp_pool, PagePool) else PagePool(cmp_pool, page_halves=128 * 128)
+    if isinstance(cmp_pool, PagePool):
+        pool = cmp_pool
+    else:
+        kind = KEY_E4M3 if np.asarray(cmp_pool).dtype.itemsize == 1 else KEY_F16
+        pool = PagePool(cmp_pool, page_halves=128 * 128, kind=kind)
+    if pool.kind == KEY_E4M3 and return_scores:
+        raise ValueError("return_scores is only implemented for fp16 keys")
     pt = np.ascontiguousarray(np.asarray(cmp_page_table, dtype=np.int32))
     if pt.ndim != 2:
         raise ValueError("page table must be 2-D")
@@ -194,6 +235,8 @@ def select(q_sel, cmp_pool, cmp_page_table, token_to_request, seq_lens,
                 _ptr(qp) + lo * 8, _ptr(out) + lo * out_width * 4, out_width]
         if return_scores:
             return lib.qsa_oracle_select_scored(*args, _ptr(scores) + lo * TOPK_BLOCKS * 4)
+        if pool.kind == KEY_E4M3:
+            return lib.qsa_oracle_select_keys(args[0], args[1], KEY_E4M3, *args[2:])
         return lib.qsa_oracle_select(*args)
 
     chunks = _row_chunks(R, threads)

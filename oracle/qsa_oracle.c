@@ -58,6 +58,26 @@ double qsa_oracle_half_to_double(uint16_t h)
 
 static float h2f(uint16_t h) { return (float)qsa_oracle_half_to_double(h); }
 
+/* OCP FP8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+ * no infinities, S.1111.111 is NaN; max 448.  Every value is exactly
+ * representable in binary16 and binary32.  The optional e4m3 compressed
+ * indexer cache of qsa_cache.py (QSAStateBackend's fp8 cache dtypes) stores
+ * its keys this way. */
+double qsa_oracle_e4m3_to_double(uint8_t v)
+{
+    int sign = (v >> 7) & 1;
+    int exp = (v >> 3) & 0xf;
+    int man = v & 0x7;
+    double x;
+    if (exp == 0xf && man == 0x7)
+        x = NAN;
+    else if (exp == 0)
+        x = ldexp((double)man, -9);                 /* subnormal: man/8 * 2^-6 */
+    else
+        x = ldexp((double)(man | 0x8), exp - 10);   /* 1.man * 2^(exp-7) */
+    return sign ? -x : x;
+}
+
 /* floor division for possibly negative numerators, positive divisor */
 static int64_t floor_div(int64_t a, int64_t b)
 {
@@ -100,7 +120,8 @@ int64_t qsa_oracle_tail_end(int64_t seq_len, int64_t pos)
  * Every non-positive head contributes +0, so s >= +0 and equal sums compare
  * equal bit for bit.
  */
-float qsa_oracle_score(const uint16_t* q, const uint16_t* k)
+/* The canonical order over binary32 key values kf[128] (exact decodes). */
+static float score_values(const uint16_t* q, const float* kf)
 {
     float r[SEL_HEADS];
     for (int h = 0; h < SEL_HEADS; ++h) {
@@ -111,8 +132,8 @@ float qsa_oracle_score(const uint16_t* q, const uint16_t* k)
             for (int j = 0; j < 16; ++j) {
                 int de = 32 * t + 2 * j;
                 int d_o = de + 1;
-                float pe = h2f(qh[de]) * h2f(k[de]);    /* exact */
-                float po = h2f(qh[d_o]) * h2f(k[d_o]);  /* exact */
+                float pe = h2f(qh[de]) * kf[de];    /* exact */
+                float po = h2f(qh[d_o]) * kf[d_o];  /* exact */
                 E = E + pe;
                 O = O + po;
             }
@@ -122,6 +143,20 @@ float qsa_oracle_score(const uint16_t* q, const uint16_t* k)
         r[h] = d > 0.0f ? d : 0.0f;
     }
     return (r[0] + r[1]) + (r[2] + r[3]);
+}
+
+float qsa_oracle_score(const uint16_t* q, const uint16_t* k)
+{
+    float kf[SEL_DIM];
+    for (int i = 0; i < SEL_DIM; ++i) kf[i] = h2f(k[i]);
+    return score_values(q, kf);
+}
+
+float qsa_oracle_score_e4m3(const uint16_t* q, const uint8_t* k)
+{
+    float kf[SEL_DIM];
+    for (int i = 0; i < SEL_DIM; ++i) kf[i] = (float)qsa_oracle_e4m3_to_double(k[i]);
+    return score_values(q, kf);
 }
 
 typedef struct {
@@ -142,7 +177,7 @@ static int cand_cmp(const void* x, const void* y)
 }
 
 /* One row of selection ([P1] Summary bullet 3, Exact contracts/Selection). */
-static uint32_t select_row(const uint16_t* q, const uint16_t* const* cmp_pages,
+static uint32_t select_row(const uint16_t* q, int key_kind, const void* const* cmp_pages,
                            int64_t num_cmp_pages, const int32_t* cmp_pt,
                            int64_t num_reqs, int64_t max_pages, int64_t pt_stride0,
                            int32_t req, const int32_t* seq_lens, int64_t pos,
@@ -169,8 +204,12 @@ static uint32_t select_row(const uint16_t* q, const uint16_t* const* cmp_pages,
             err |= QSA_ORACLE_ERR_CMP_PAGE;
             continue;
         }
-        const uint16_t* key = cmp_pages[pg] + (b % CMP_PAGE_KEYS) * SEL_DIM;
-        c[n].s = qsa_oracle_score(q, key);
+        if (key_kind == QSA_ORACLE_KEY_E4M3)
+            c[n].s = qsa_oracle_score_e4m3(
+                q, (const uint8_t*)cmp_pages[pg] + (b % CMP_PAGE_KEYS) * SEL_DIM);
+        else
+            c[n].s = qsa_oracle_score(
+                q, (const uint16_t*)cmp_pages[pg] + (b % CMP_PAGE_KEYS) * SEL_DIM);
         c[n].b = b;
         ++n;
     }
@@ -189,8 +228,8 @@ static uint32_t select_row(const uint16_t* q, const uint16_t* const* cmp_pages,
     return err;
 }
 
-static uint32_t select_rows(int64_t R, const uint16_t* q_sel,
-                            const uint16_t* const* cmp_pages, int64_t num_cmp_pages,
+static uint32_t select_rows(int64_t R, const uint16_t* q_sel, int key_kind,
+                            const void* const* cmp_pages, int64_t num_cmp_pages,
                             const int32_t* cmp_pt, int64_t num_reqs, int64_t max_pages,
                             int64_t pt_stride0, const int32_t* t2r,
                             const int32_t* seq_lens, const int64_t* qpos,
@@ -199,7 +238,7 @@ static uint32_t select_rows(int64_t R, const uint16_t* q_sel,
     uint32_t err = 0;
     if (out_width < OUT_WIDTH) return 0xffffffffu;
     for (int64_t r = 0; r < R; ++r)
-        err |= select_row(q_sel + r * SEL_HEADS * SEL_DIM, cmp_pages, num_cmp_pages,
+        err |= select_row(q_sel + r * SEL_HEADS * SEL_DIM, key_kind, cmp_pages, num_cmp_pages,
                           cmp_pt, num_reqs, max_pages, pt_stride0, t2r[r], seq_lens,
                           qpos[r], out + r * out_width, out_width,
                           scores_out ? scores_out + r * TOPK_BLOCKS : NULL);
@@ -213,7 +252,20 @@ uint32_t qsa_oracle_select(int64_t R, const uint16_t* q_sel,
                            const int32_t* seq_lens, const int64_t* qpos,
                            int32_t* out, int64_t out_width)
 {
-    return select_rows(R, q_sel, cmp_pages, num_cmp_pages, cmp_pt, num_reqs, max_pages,
+    return select_rows(R, q_sel, QSA_ORACLE_KEY_F16, (const void* const*)cmp_pages,
+                       num_cmp_pages, cmp_pt, num_reqs, max_pages, pt_stride0, t2r, seq_lens,
+                       qpos, out, out_width, NULL);
+}
+
+uint32_t qsa_oracle_select_keys(int64_t R, const uint16_t* q_sel, int key_kind,
+                                const void* const* cmp_pages, int64_t num_cmp_pages,
+                                const int32_t* cmp_pt, int64_t num_reqs, int64_t max_pages,
+                                int64_t pt_stride0, const int32_t* t2r,
+                                const int32_t* seq_lens, const int64_t* qpos,
+                                int32_t* out, int64_t out_width)
+{
+    if (key_kind != QSA_ORACLE_KEY_F16 && key_kind != QSA_ORACLE_KEY_E4M3) return 0xffffffffu;
+    return select_rows(R, q_sel, key_kind, cmp_pages, num_cmp_pages, cmp_pt, num_reqs, max_pages,
                        pt_stride0, t2r, seq_lens, qpos, out, out_width, NULL);
 }
 
@@ -224,8 +276,9 @@ uint32_t qsa_oracle_select_scored(int64_t R, const uint16_t* q_sel,
                                   const int32_t* seq_lens, const int64_t* qpos,
                                   int32_t* out, int64_t out_width, float* scores_out)
 {
-    return select_rows(R, q_sel, cmp_pages, num_cmp_pages, cmp_pt, num_reqs, max_pages,
-                       pt_stride0, t2r, seq_lens, qpos, out, out_width, scores_out);
+    return select_rows(R, q_sel, QSA_ORACLE_KEY_F16, (const void* const*)cmp_pages,
+                       num_cmp_pages, cmp_pt, num_reqs, max_pages, pt_stride0, t2r, seq_lens,
+                       qpos, out, out_width, scores_out);
 }
 
 /*

@@ -41,6 +41,14 @@ extern "C" {
 /* fp16 bits -> binary64 (exact). */
 double qsa_oracle_half_to_double(uint16_t h);
 
+/* OCP FP8 E4M3 ("fn": no infinities; S.1111.111 is NaN) bits -> binary64
+ * (exact). */
+double qsa_oracle_e4m3_to_double(uint8_t v);
+
+/* compressed-key element types */
+#define QSA_ORACLE_KEY_F16   0
+#define QSA_ORACLE_KEY_E4M3  1
+
 /* Canonical binary32 selection score of one compressed key against the four
  * indexer heads: sum over h of ReLU(q_h . k).  q: [4][128] fp16 bits,
  * k: [128] fp16 bits.  The summation order is fixed (see the .c file). */
@@ -66,6 +74,19 @@ uint32_t qsa_oracle_select(int64_t R, const uint16_t* q_sel,
                            int64_t pt_stride0, const int32_t* t2r,
                            const int32_t* seq_lens, const int64_t* qpos,
                            int32_t* out, int64_t out_width);
+
+/* Selection with the compressed keys stored as key_kind elements (page p ->
+ * [128 keys][128] elements of that type); QSA_ORACLE_KEY_F16 is
+ * qsa_oracle_select. */
+uint32_t qsa_oracle_select_keys(int64_t R, const uint16_t* q_sel, int key_kind,
+                                const void* const* cmp_pages, int64_t num_cmp_pages,
+                                const int32_t* cmp_pt, int64_t num_reqs, int64_t max_pages,
+                                int64_t pt_stride0, const int32_t* t2r,
+                                const int32_t* seq_lens, const int64_t* qpos,
+                                int32_t* out, int64_t out_width);
+
+/* Canonical score of an E4M3 key [128] (same order as qsa_oracle_score). */
+float qsa_oracle_score_e4m3(const uint16_t* q, const uint8_t* k);
 
 /* Same, but also returns the binary32 score of every selected block in the
  * order emitted (scores_out [R][512], unused entries -1.0f) -- used by tests

@@ -71,9 +71,10 @@ class Workload:
         return Workload(**kw)
 
 
-def _fill_normal(shape, std: float, gen: torch.Generator, device) -> torch.Tensor:
-    """fp32 N(0, std^2) draws rounded to fp16, filled chunk by chunk."""
-    out = torch.empty(shape, dtype=torch.float16, device=device)
+def _fill_normal(shape, std: float, gen: torch.Generator, device,
+                 dtype=torch.float16) -> torch.Tensor:
+    """fp32 N(0, std^2) draws rounded to `dtype`, filled chunk by chunk."""
+    out = torch.empty(shape, dtype=dtype, device=device)
     flat = out.view(-1)
     n = flat.numel()
     for s in range(0, n, _CHUNK):
@@ -100,7 +101,7 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
           cmp_std: float = 0.1, distinct_keys: int = 0,
           dup_mapping: bool = False, premade_widths: list[int] | None = None,
           hole_frac: float = 0.10, dup_frac: float = 0.05,
-          seed: int = 0, device="cpu") -> Workload:
+          cmp_dtype: str = "fp16", seed: int = 0, device="cpu") -> Workload:
     """General builder: one request per row (token_to_request = arange(R)).
 
     ``positions`` default to seq_len-1 (plain decode).  Each request gets the
@@ -112,8 +113,14 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
     K/V page into two of its logical columns and request 1 map one page that
     request 0 also uses.  ``premade_widths`` builds attention index lists
     (valid widths cycled over rows; holes and duplicates as in the stress
-    workload) instead of relying on the selection output.
+    workload) instead of relying on the selection output.  ``cmp_dtype``
+    "fp8" stores the compressed keys as FP8 E4M3 (torch.float8_e4m3fn, the
+    same draws rounded to E4M3) -- the optional e4m3 compressed indexer
+    cache.
     """
+    if cmp_dtype not in ("fp16", "fp8"):
+        raise ValueError("cmp_dtype must be 'fp16' or 'fp8'")
+    kdt = torch.float8_e4m3fn if cmp_dtype == "fp8" else torch.float16
     R = len(seq_lens)
     sg = torch.Generator().manual_seed(seed)
     if positions is None:
@@ -174,11 +181,12 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
     vg = torch.Generator(device=device).manual_seed(seed + 1)
     q_sel = _fill_normal((R, SEL_HEADS, SEL_DIM), 1.0, vg, device)
     if distinct_keys:
-        vecs = _fill_normal((distinct_keys, SEL_DIM), cmp_std, vg, device)
+        vecs = _fill_normal((distinct_keys, SEL_DIM), cmp_std, vg, device, kdt)
         pick = torch.randint(0, distinct_keys, (cmp_pool * CMP_PAGE,), generator=sg)
-        cmp = vecs[pick.to(device)].view(cmp_pool, CMP_PAGE, 1, SEL_DIM).contiguous()
+        cmp = vecs.view(torch.uint8 if kdt != torch.float16 else kdt)[pick.to(device)]
+        cmp = cmp.view(kdt).view(cmp_pool, CMP_PAGE, 1, SEL_DIM).contiguous()
     else:
-        cmp = _fill_normal((cmp_pool, CMP_PAGE, 1, SEL_DIM), cmp_std, vg, device)
+        cmp = _fill_normal((cmp_pool, CMP_PAGE, 1, SEL_DIM), cmp_std, vg, device, kdt)
     q_attn = _fill_normal((R, ATT_HEADS, ATT_DIM), 1.0, vg, device)
     kv = _fill_normal((kv_pool, KV_PAGE, 2, ATT_DIM), 1.0, vg, device)
 
@@ -204,7 +212,8 @@ CONFIG_NAMES = {
 }
 
 
-def config(cfg: int, device="cpu", seed: int | None = None, rows: int | None = None) -> Workload:
+def config(cfg: int, device="cpu", seed: int | None = None, rows: int | None = None,
+           cmp_dtype: str = "fp16") -> Workload:
     """The five workloads (seed 1000+cfg unless given).  ``rows`` truncates a
     multi-row workload to its first rows (structure drawn for all rows first,
     so the kept rows are identical to the full workload's structure) -- only
@@ -214,18 +223,19 @@ def config(cfg: int, device="cpu", seed: int | None = None, rows: int | None = N
     if cfg == 0:
         # 519 tokens: 129 visible blocks over 2 compressed pages + 3-token tail;
         # pools of 8 compressed / 4 K/V pages, tables a permutation of the pool.
-        return _permuted_single(name, 519, 8, 4, seed, device)
+        return _permuted_single(name, 519, 8, 4, seed, device, cmp_dtype)
     if cfg == 1:
         # 9215 tokens: 2303 visible blocks (18 pages) in a pool of 8192;
         # K/V pool of 64 pages, 18 in use.
-        return build(name, [9215], cmp_pool=8192, kv_pool=64, seed=seed, device=device)
+        return build(name, [9215], cmp_pool=8192, kv_pool=64, cmp_dtype=cmp_dtype, seed=seed,
+                     device=device)
     if cfg == 2:
         sg = torch.Generator().manual_seed(seed + 7)
         L = _randint(512, 65536, 64, sg)
         if rows:
             L = L[:rows]
         return build(name, L, cmp_pool=16384, kv_pool=8192, cmp_cols=128, kv_cols=128,
-                     seed=seed, device=device)
+                     cmp_dtype=cmp_dtype, seed=seed, device=device)
     if cfg == 3:
         sg = torch.Generator().manual_seed(seed + 7)
         L = _randint(300, 20000, 16, sg)
@@ -235,22 +245,23 @@ def config(cfg: int, device="cpu", seed: int | None = None, rows: int | None = N
         need_k = sum(_pages_for(x, KV_PAGE) for x in L)
         return build(name, L, cmp_pool=need_c + 16, kv_pool=need_k + 16, distinct_keys=4,
                      dup_mapping=True, premade_widths=[0, 1, 32, 1024, 2051],
-                     seed=seed, device=device)
+                     cmp_dtype=cmp_dtype, seed=seed, device=device)
     if cfg == 4:
         R = rows or 256
         return build(name, [131072] * R, cmp_pool=256 * R, kv_pool=256 * R,
-                     seed=seed, device=device)
+                     cmp_dtype=cmp_dtype, seed=seed, device=device)
     raise ValueError(f"unknown workload {cfg}")
 
 
-def _permuted_single(name, L, cmp_pool, kv_pool, seed, device) -> Workload:
+def _permuted_single(name, L, cmp_pool, kv_pool, seed, device, cmp_dtype="fp16") -> Workload:
     """One row whose page tables are full random permutations of small pools."""
     sg = torch.Generator().manual_seed(seed)
     cmp_pt = torch.randperm(cmp_pool, generator=sg).to(torch.int32).view(1, -1)
     kv_pt = torch.randperm(kv_pool, generator=sg).to(torch.int32).view(1, -1)
     vg = torch.Generator(device=device).manual_seed(seed + 1)
     q_sel = _fill_normal((1, SEL_HEADS, SEL_DIM), 1.0, vg, device)
-    cmp = _fill_normal((cmp_pool, CMP_PAGE, 1, SEL_DIM), 0.1, vg, device)
+    kdt = torch.float8_e4m3fn if cmp_dtype == "fp8" else torch.float16
+    cmp = _fill_normal((cmp_pool, CMP_PAGE, 1, SEL_DIM), 0.1, vg, device, kdt)
     q_attn = _fill_normal((1, ATT_HEADS, ATT_DIM), 1.0, vg, device)
     kv = _fill_normal((kv_pool, KV_PAGE, 2, ATT_DIM), 1.0, vg, device)
     return Workload(
