@@ -83,6 +83,12 @@ def select_bytes_per_row(seq_len: int, pos: int) -> int:
     return 256 * V + 4 * 128 * 2 + 4 * math.ceil(V / 128) + 4 * 2051 + 4 + 4 + 8
 
 
+def select_bytes_per_row_fp8(seq_len: int, pos: int) -> int:
+    """select_bytes_per_row with 1-byte (E4M3) compressed keys."""
+    V = max(0, min((pos + 1) // 4, seq_len // 4))
+    return 128 * V + 4 * 128 * 2 + 4 * math.ceil(V / 128) + 4 * 2051 + 4 + 4 + 8
+
+
 def attend_bytes_per_row(idx_row: np.ndarray) -> int:
     """distinct valid tokens (1 KiB K+V each) + q + out + index read + the
     K/V page-table entries touched + request id."""
@@ -382,6 +388,9 @@ def run_ours(args, world, rank, local):
         raise SystemExit(f"bench.py: device error word {int(err.item())}")
 
     peak, peak_kind = _peaks()
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak)
     sel_gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
     att_gbs = att_bytes / (att_ms * 1e-3) / 1e9
     step_gbs = (sel_bytes + att_bytes) / (total_ms / K * 1e-3) / 1e9
@@ -420,11 +429,58 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms, "steps": Ke},
+        "fp8_compressed_cache": fp8,
         "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak):
+    """The same decode step with the compressed keys stored as FP8 E4M3 (the
+    optional e4m3 compressed indexer cache): the same draws rounded to E4M3,
+    K/V and everything else shared.  Timed like the main measurement."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    cmp8 = w.cmp_cache.to(torch.float8_e4m3fn)
+    sel_ws = torch.empty(qsa.qsa_select_workspace_bytes(R, w.cmp_page_table.shape[1]),
+                         dtype=torch.uint8, device=dev)
+
+    def step():
+        qsa.qsa_select_paged_tokens(w.q_sel, cmp8, w.cmp_page_table, w.token_to_request,
+                                    w.seq_lens, w.query_positions, out=idx, workspace=sel_ws,
+                                    error_word=err, stream=stream)
+        e_mid.record(stream) if e_mid is not None else None
+        qsa.qsa_sparse_attention(w.q_attn, w.k_view, w.v_view, w.kv_page_table,
+                                 w.token_to_request, idx, out=out, workspace=att_ws,
+                                 error_word=err, stream=stream)
+
+    e_mid = None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(1, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    for i in range(K):
+        ev[i][0].record(stream)
+        e_mid = ev[i][1]
+        step()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    total = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_step = max_over_ranks(total, world, dev)
+    seq = w.seq_lens.cpu().numpy()
+    pos = w.query_positions.cpu().numpy()
+    t2r = w.token_to_request.cpu().numpy()
+    sel_bytes = sum(select_bytes_per_row_fp8(int(seq[t2r[r]]), int(pos[r])) for r in range(R))
+    gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
+    del cmp8
+    return {"value": R * world / (t_step * 1e-3), "unit": "rows/s", "ms_per_step": t_step,
+            "steps": K, "select_ms": sel_ms, "select_hbm_gbs": gbs, "select_frac": gbs / peak,
+            "select_algorithmic_bytes": sel_bytes}
 
 
 def main():
@@ -438,6 +494,8 @@ def main():
                     help="keep only the first rows of a multi-row workload (profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the FP8-E4M3 compressed-cache measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps are required")

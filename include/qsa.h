@@ -82,6 +82,7 @@ typedef int qsa_dtype;
 #define QSA_DT_F32   3
 #define QSA_DT_I32   4
 #define QSA_DT_I64   5
+#define QSA_DT_F8E4M3 6   /* OCP FP8 E4M3 ("fn"): compressed keys only */
 
 /* Device-detected data errors, ORed into *error_word (never cleared by the
  * library; the caller zeroes it when it wants a fresh reading). */
@@ -124,9 +125,13 @@ QSA_API size_t qsa_select_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols)
  * Arguments
  *   q_sel            FP16 [num_rows,4,128], strides q_sel_strides (must be
  *                    {512,128,1}: contiguous)
- *   cmp_cache        FP16 [P,128,1,128], shape cmp_shape, strides cmp_strides
- *                    (must be {16384,128,*,1}; the size-1 dim's stride is
- *                    ignored)
+ *   cmp_cache        [P,128,1,128], shape cmp_shape, strides cmp_strides in
+ *                    elements (must be {16384,128,*,1}; the size-1 dim's
+ *                    stride is ignored).  cmp_dtype QSA_DT_F16, or
+ *                    QSA_DT_F8E4M3 for the optional e4m3 compressed indexer
+ *                    cache (qsa_cache.py, QSAStateBackend cache dtypes): each
+ *                    key element is decoded exactly (E4M3 values are exact in
+ *                    fp16) and scored by the same rule and order.
  *   cmp_page_table   int32 [num_reqs, cmp_pt_cols], row stride cmp_pt_stride0
  *                    (elements, >= cmp_pt_cols), column stride 1
  *   token_to_request int32 [num_rows]

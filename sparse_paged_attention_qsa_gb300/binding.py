@@ -25,9 +25,9 @@ TOPK_BLOCKS = 512
 OUT_WIDTH = 2051
 DERR_REQUEST, DERR_CMP_PAGE, DERR_KV_PAGE, DERR_TIMEOUT = 1, 2, 4, 8
 
-DT_F16, DT_BF16, DT_F32, DT_I32, DT_I64 = 1, 2, 3, 4, 5
+DT_F16, DT_BF16, DT_F32, DT_I32, DT_I64, DT_F8E4M3 = 1, 2, 3, 4, 5, 6
 _DTYPE_TAG = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_F32,
-              torch.int32: DT_I32, torch.int64: DT_I64}
+              torch.int32: DT_I32, torch.int64: DT_I64, torch.float8_e4m3fn: DT_F8E4M3}
 
 STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE",
           4: "QSA_ERR_STRIDE", 5: "QSA_ERR_ALIGN", 6: "QSA_ERR_CONTRACT",

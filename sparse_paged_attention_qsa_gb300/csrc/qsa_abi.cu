@@ -81,7 +81,9 @@ qsa_status qsa_select_paged_tokens(
   // contract constants and dtypes ("Exact contracts" / Selection)
   if (token_topk != qsa::kTokenTopk || compress_ratio != qsa::kRatio) return QSA_ERR_CONTRACT;
   if (out_width != qsa::kOutWidth) return QSA_ERR_CONTRACT;
-  if (q_sel_dtype != QSA_DT_F16 || cmp_dtype != QSA_DT_F16) return QSA_ERR_DTYPE;
+  if (q_sel_dtype != QSA_DT_F16) return QSA_ERR_DTYPE;
+  if (cmp_dtype != QSA_DT_F16 && cmp_dtype != QSA_DT_F8E4M3) return QSA_ERR_DTYPE;
+  const int64_t cmp_esize = cmp_dtype == QSA_DT_F16 ? 2 : 1;
   if (cmp_pt_dtype != QSA_DT_I32 || t2r_dtype != QSA_DT_I32 || seq_lens_dtype != QSA_DT_I32)
     return QSA_ERR_DTYPE;
   if (qpos_dtype != QSA_DT_I64 || out_dtype != QSA_DT_I32) return QSA_ERR_DTYPE;
@@ -120,7 +122,7 @@ qsa_status qsa_select_paged_tokens(
   const Span o = span(out_indices, ((num_rows - 1) * out_stride0 + out_width) * 4);
   const Span ins[] = {
       span(q_sel, num_rows * kSelHeads * kSelDim * 2),
-      span(cmp_cache, cmp_shape[0] * kCmpPageKeys * kSelDim * 2),
+      span(cmp_cache, cmp_shape[0] * kCmpPageKeys * kSelDim * cmp_esize),
       span(cmp_page_table, ((num_reqs - 1) * cmp_pt_stride0 + cmp_pt_cols) * 4),
       span(token_to_request, num_rows * 4),
       span(seq_lens, num_reqs * 4),
@@ -138,7 +140,8 @@ qsa_status qsa_select_paged_tokens(
 
   qsa::SelectParams p{};
   p.q_sel = static_cast<const __half*>(q_sel);
-  p.cmp = static_cast<const __half*>(cmp_cache);
+  p.cmp = cmp_cache;
+  p.key_fp8 = cmp_dtype == QSA_DT_F8E4M3 ? 1 : 0;
   p.num_pages = cmp_shape[0];
   p.pt = static_cast<const int32_t*>(cmp_page_table);
   p.num_reqs = num_reqs;

@@ -34,7 +34,8 @@ constexpr uint32_t kErrTimeout = 8u;
 
 struct SelectParams {
   const __half* q_sel;        // [R,4,128]
-  const __half* cmp;          // [P,128,1,128], page stride 16384 halves
+  const void* cmp;            // [P,128,1,128] fp16 or E4M3, page stride 16384 elements
+  int key_fp8;                // 1: E4M3 keys, 0: fp16 keys
   int64_t num_pages;
   const int32_t* pt;          // [num_reqs, pt_cols], row stride pt_stride0
   int64_t num_reqs, pt_cols, pt_stride0;

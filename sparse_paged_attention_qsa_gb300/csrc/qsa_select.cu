@@ -36,8 +36,16 @@ namespace qsa {
 namespace {
 
 // score kernel: persistent, one CTA per SM, warp-specialised
-constexpr int kStages = 6;                              // 6 x 32 KiB pages in flight per SM
-constexpr int kPageBytes = kCmpPageKeys * kSelDim * 2;  // one compressed page
+// The ring holds kRingBytes of pages: 6 fp16 pages (32 KiB) or 12 E4M3 pages
+// (16 KiB).  KeyCfg gives the per-key-type sizes.
+constexpr int kRingBytes = 6 * kCmpPageKeys * kSelDim * 2;   // 192 KiB in flight per SM
+constexpr int kMaxStages = 12;
+template <bool kFp8>
+struct KeyCfg {
+  static constexpr int kPageBytes = kCmpPageKeys * kSelDim * (kFp8 ? 1 : 2);
+  static constexpr int kStages = kRingBytes / kPageBytes;
+  static constexpr int kRowsPerKey = kFp8 ? 1 : 2;            // 128-byte TMA rows per key
+};
 #ifndef QSA_SCORE_WARPS
 #define QSA_SCORE_WARPS 8
 #endif
@@ -45,8 +53,8 @@ constexpr int kScoreWarps = QSA_SCORE_WARPS;            // consumer warps: 8 or 
 constexpr int kScoreThreads = (kScoreWarps + 1) * 32;   // + one producer warp
 constexpr int kScoreGroups = 16 / kScoreWarps;          // groups of 8 keys per warp per page
 constexpr int kMaxRows = 2048;                          // rows per launch (row tables in smem)
-constexpr size_t kScoreSmem = (size_t)kStages * kPageBytes + 1024 + 2 * kStages * 8 +
-                              kStages * 16 + 3 * kMaxRows * sizeof(int);
+constexpr size_t kScoreSmem = (size_t)kRingBytes + 1024 + 2 * kMaxStages * 8 +
+                              kMaxStages * 16 + 3 * kMaxRows * sizeof(int);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s: any wait longer is a fault
 
 constexpr int kTopkThreads = 512;                       // one key per thread in the sort
@@ -147,6 +155,22 @@ __device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float 
   return d;
 }
 
+// Two E4M3 values (low byte = even dim) -> fp16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t v) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+      : "=r"(d) : "r"(v));
+  return d;
+}
+
+// 16 E4M3 values (one 16-byte chunk) -> 16 fp16 values as two 16-byte words.
+__device__ __forceinline__ void e4m3x16_to_h(uint4 c, uint4& lo, uint4& hi) {
+  lo = make_uint4(e4m3x2_to_h2(c.x & 0xffffu), e4m3x2_to_h2(c.x >> 16),
+                  e4m3x2_to_h2(c.y & 0xffffu), e4m3x2_to_h2(c.y >> 16));
+  hi = make_uint4(e4m3x2_to_h2(c.z & 0xffffu), e4m3x2_to_h2(c.z >> 16),
+                  e4m3x2_to_h2(c.w & 0xffffu), e4m3x2_to_h2(c.w >> 16));
+}
+
 // Score of one key held as four 32-dim slices by a quad of lanes, reduced in
 // the canonical order; returns the ordered key bits(s)+1 on every lane.
 // q: this lane's slice of the 4 heads as fp16 pairs (dims 32t+2j, 32t+2j+1);
@@ -212,8 +236,11 @@ struct StageDesc {
 // 2k + t/2, 16-byte chunks (4(t&1)+j) XOR (row & 7): the 8 lanes of each
 // shared-memory phase hit 8 distinct bank groups, and each lane reads its
 // slice in ascending order.
+template <bool kFp8>
 __global__ void __launch_bounds__(kScoreThreads, 1)
 score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
+  constexpr int kPageBytes = KeyCfg<kFp8>::kPageBytes;
+  constexpr int kStages = KeyCfg<kFp8>::kStages;
   extern __shared__ unsigned char smem_raw[];
   __shared__ int s_abort;
   __shared__ int64_t s_total;
@@ -221,11 +248,11 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   const uint32_t base = raw + pad;
-  const uint32_t bar_full = base + kStages * kPageBytes;
-  const uint32_t bar_empty = bar_full + kStages * 8;
+  const uint32_t bar_full = base + kRingBytes;
+  const uint32_t bar_empty = bar_full + kMaxStages * 8;
   unsigned char* gbase = smem_raw + pad;
-  StageDesc* desc = reinterpret_cast<StageDesc*>(gbase + kStages * kPageBytes + 2 * kStages * 8);
-  int* row_req = reinterpret_cast<int*>(desc + kStages);
+  StageDesc* desc = reinterpret_cast<StageDesc*>(gbase + kRingBytes + 2 * kMaxStages * 8);
+  int* row_req = reinterpret_cast<int*>(desc + kMaxStages);
   int* row_vs = row_req + kMaxRows;
   int* row_pre = row_vs + kMaxRows;          // exclusive prefix of page counts
   const int tid = threadIdx.x;
@@ -347,8 +374,8 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
         ++issued;
         if (pg >= 0) {
           mbar_expect_tx(bar_full + 8 * s, kPageBytes);
-          tma_load_2d(base + s * kPageBytes, &tmap, 0, pg * 2 * kCmpPageKeys, bar_full + 8 * s,
-                      policy);
+          tma_load_2d(base + s * kPageBytes, &tmap, 0, pg * KeyCfg<kFp8>::kRowsPerKey * kCmpPageKeys,
+                      bar_full + 8 * s, policy);
         } else {                    // range done: mark the stage as the end
           desc[s].row = -1;
           mbar_arrive(bar_full + 8 * s);
@@ -395,12 +422,25 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
       for (int g = 0; g < kScoreGroups; ++g) {
         const int k = (warp * kScoreGroups + g) * 8 + kslot;
-        const uint32_t row = 2 * k + (t >> 1);
-        const uint32_t rbase = stage + row * 128;
+        if (kFp8) {
+          // one 128-byte row per key; slice t = 16-byte chunks 2t, 2t+1
+          const uint32_t row = (uint32_t)k;
+          const uint32_t rbase = stage + row * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
-          kv[g][j] = lds128(rbase + chunk * 16);
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t chunk = (uint32_t)(2 * t + j) ^ (row & 7u);
+            const uint4 c = lds128(rbase + chunk * 16);
+            e4m3x16_to_h(c, kv[g][2 * j], kv[g][2 * j + 1]);
+          }
+        } else {
+          // two 128-byte rows per key; slice t = row 2k + t/2, chunks 4(t&1)+j
+          const uint32_t row = 2 * k + (t >> 1);
+          const uint32_t rbase = stage + row * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
+            kv[g][j] = lds128(rbase + chunk * 16);
+          }
         }
       }
 #pragma unroll
@@ -767,19 +807,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view of the compressed cache: rows of 64 halves (128 B), two rows per
-// key, 256 rows per page; one box = one page; 128-byte swizzle.
+// 2-D view of the compressed cache in 128-byte rows: fp16 keys are two rows
+// of 64 halves (256 rows per page), E4M3 keys one row of 128 bytes (128 rows
+// per page); one box = one page; 128-byte swizzle.
 cudaError_t encode_cmp_map(const SelectParams& p, CUtensorMap* map) {
   memset(map, 0, sizeof(*map));
   if (p.num_pages <= 0) return cudaSuccess;   // no page can be loaded
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {64, (cuuint64_t)p.num_pages * 2 * kCmpPageKeys};
+  const bool fp8 = p.key_fp8 != 0;
+  const cuuint32_t rows_per_page = (fp8 ? 1 : 2) * kCmpPageKeys;
+  cuuint64_t dims[2] = {fp8 ? 128u : 64u, (cuuint64_t)p.num_pages * rows_per_page};
   cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {64, 2 * kCmpPageKeys};
+  cuuint32_t box[2] = {fp8 ? 128u : 64u, rows_per_page};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(p.cmp), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                  const_cast<void*>(p.cmp), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -801,7 +845,10 @@ cudaError_t device_info(DeviceInfo** out) {
   if (!d.smem_set) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScoreSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScoreSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -834,7 +881,10 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     c.scores = p.scores + (int64_t)r0 * p.vcap;
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
-    score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
+    if (c.key_fp8)
+      score_kernel<true><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
+    else
+      score_kernel<false><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
     e = launch_after(topk_kernel, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c);
     if (e != cudaSuccess) return e;
   }

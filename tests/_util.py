@@ -9,13 +9,17 @@ import oracle
 
 def _pool(cache: torch.Tensor, page_ids, page_halves: int) -> "oracle.PagePool":
     P = cache.shape[0]
+    kind = oracle.KEY_E4M3 if cache.dtype == torch.float8_e4m3fn else oracle.KEY_F16
     ids = sorted({int(p) for p in page_ids if 0 <= int(p) < P})
     if not ids:
-        return oracle.PagePool({}, num_pages=P)
+        return oracle.PagePool({}, num_pages=P, kind=kind)
     sel = torch.tensor(ids, dtype=torch.long, device=cache.device)
-    host = cache.index_select(0, sel).cpu().numpy().reshape(len(ids), -1)
+    pages = cache.index_select(0, sel)
+    if kind == oracle.KEY_E4M3:
+        pages = pages.view(torch.uint8)
+    host = pages.cpu().numpy().reshape(len(ids), -1)
     return oracle.PagePool({p: host[i] for i, p in enumerate(ids)}, num_pages=P,
-                           page_halves=page_halves)
+                           page_halves=page_halves, kind=kind)
 
 
 def _req_pages(pt: np.ndarray, t2r: np.ndarray, rows):

@@ -98,7 +98,8 @@ def _sel(lib, **over):
 
 @pytest.mark.parametrize("over,status", [
     (dict(topk=1024), 6), (dict(ratio=8), 6), (dict(ow=2048), 6),
-    (dict(qdt=3), 2), (dict(qdt=2), 2), (dict(cdt=2), 2), (dict(ptdt=5), 2),
+    (dict(qdt=3), 2), (dict(qdt=2), 2), (dict(cdt=2), 2), (dict(cdt=5), 2), (dict(ptdt=5), 2),
+    (dict(cdt=6, ws=None), 7),   # E4M3 keys pass the dtype check (then: no workspace)
     (dict(t2rdt=5), 2), (dict(sldt=5), 2), (dict(qpdt=4), 2), (dict(odt=5), 2),
     (dict(R=70000), 3), (dict(R=-1), 3),
     (dict(cshape=_arr([64, 64, 1, 128])), 3), (dict(cshape=_arr([64, 128, 2, 128])), 3),

@@ -167,3 +167,43 @@ def test_select_fail_closed_dtypes_and_output():
     with pytest.raises(qsa.QSAError) as e:           # non-contiguous query
         qsa.qsa_select_paged_tokens(w.q_sel.transpose(1, 2).contiguous().transpose(1, 2), *args[1:])
     assert e.value.status == 4
+
+
+# --- FP8-E4M3 compressed keys (qsa_cache.py: the optional e4m3 compressed
+# indexer cache); same score rule and order, bit-exact indices ---------------
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_select_fp8_configs(cfg):
+    w = W.config(cfg, device=DEV, cmp_dtype="fp8")
+    assert w.cmp_cache.dtype == torch.float8_e4m3fn
+    _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
+def test_select_fp8_config4_sampled_rows():
+    w = W.config(4, device=DEV, cmp_dtype="fp8")
+    got, gerr = _gpu(w)
+    assert gerr == 0
+    rows = [0, 129, 255]
+    exp, _ = oracle_select(w, rows=rows)
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[r], exp[i]), r
+    assert (got[:, :2048] >= 0).all() and (got[:, 2048:] == -1).all()
+
+
+def test_select_fp8_edges_ties_and_bad_pages():
+    w = W.build("fp8edge", [0, 3, 515, 4099, 30001], distinct_keys=4, dup_mapping=True,
+                cmp_dtype="fp8", seed=41, device=DEV)
+    pt = w.cmp_page_table.clone()
+    pt[3, 5] = w.cmp_cache.shape[0] + 1
+    got, gerr, oerr = _check(w, pt=pt)
+    assert gerr == oerr == qsa.DERR_CMP_PAGE
+
+
+def test_select_fp8_matches_fp16_on_identical_values():
+    # E4M3 keys and the same values stored as fp16 must select identically
+    w8 = W.build("same", [20003, 777], cmp_dtype="fp8", seed=42, device=DEV)
+    w16 = W.Workload(**{**w8.__dict__, "cmp_cache": w8.cmp_cache.to(torch.float16)})
+    a, _ = _gpu(w8)
+    b, _ = _gpu(w16)
+    assert np.array_equal(a, b)
