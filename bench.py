@@ -391,6 +391,10 @@ def run_ours(args, world, rank, local):
     fp8 = None
     if not args.no_fp8:
         fp8 = fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak)
+    meta = metadata_timing(args, R, world, dev, stream, w.cmp_page_table, w.seq_lens)
+    spec = None
+    if not args.no_spec and args.workload == 4:
+        spec = spec_variant(args, R, world, rank, dev, stream, peak)
     sel_gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
     att_gbs = att_bytes / (att_ms * 1e-3) / 1e9
     step_gbs = (sel_bytes + att_bytes) / (total_ms / K * 1e-3) / 1e9
@@ -430,6 +434,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms, "steps": Ke},
         "fp8_compressed_cache": fp8,
+        "metadata_builder": meta,
+        "speculative_decode": spec,
         "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
@@ -483,6 +489,99 @@ def fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak):
             "select_algorithmic_bytes": sel_bytes}
 
 
+def _time_calls(fn, n, stream, dev, world):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+
+
+def metadata_timing(args, R, world, dev, stream, cmp_pt, seq):
+    """The side-cache metadata builder (one launch) on this workload's batch:
+    one query token per request, compressed-key slot map and work list."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    qsl = torch.arange(R + 1, dtype=torch.int32, device=dev)
+    common = torch.arange(R, dtype=torch.int64, device=dev)
+    outs = qsa.qsa_build_metadata(qsl, seq, cmp_pt, R, storage_block_size=128,
+                                  compress_ratio=4, common_slot_mapping=common,
+                                  num_mapped_tokens=R, max_num_work=2 * R, stream=stream)
+
+    def call():
+        qsa.qsa_build_metadata(qsl, seq, cmp_pt, R, storage_block_size=128, compress_ratio=4,
+                               common_slot_mapping=common, num_mapped_tokens=R,
+                               max_num_work=2 * R, out=outs, stream=stream)
+
+    n = 2000
+    ms = _time_calls(call, n, stream, dev, world)
+    return {"us_per_call": ms * 1e3, "tokens": R, "requests": R, "work_items": 2 * R,
+            "calls": n, "bound": "launch latency (a few KB per call)"}
+
+
+def spec_variant(args, R, world, rank, dev, stream, peak):
+    """Speculative / multi-token decode: R rows as R/4 requests x 4 query
+    tokens (positions L-4 .. L-1, L = 131072).  One step = the metadata
+    builder (token -> request, positions) + selection + attention, all on
+    the device.  Inputs drawn like the main workload (own pools)."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    nreq = max(1, R // 4)
+    w = W.build("spec_R%d_%dx4_L131072" % (4 * nreq, nreq), [131072] * nreq,
+                query_lens=[4] * nreq, cmp_pool=256 * nreq, kv_pool=256 * nreq,
+                seed=4242 + 7919 * rank, device=dev)
+    T = w.R
+    common = torch.zeros(T, dtype=torch.int64, device=dev)
+    meta = qsa.qsa_build_metadata(w.query_start_loc, w.seq_lens, w.cmp_page_table, T,
+                                  storage_block_size=128, compress_ratio=4,
+                                  common_slot_mapping=common, num_mapped_tokens=T,
+                                  stream=stream)
+    idx = torch.empty((T, 2051), dtype=torch.int32, device=dev)
+    out = torch.empty((T, 3, 256), dtype=torch.float16, device=dev)
+    sel_ws = torch.empty(qsa.qsa_select_workspace_bytes(T, w.cmp_page_table.shape[1]),
+                         dtype=torch.uint8, device=dev)
+    att_ws = torch.empty(qsa.qsa_attention_workspace_bytes(T, 2051), dtype=torch.uint8,
+                         device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        qsa.qsa_build_metadata(w.query_start_loc, w.seq_lens, w.cmp_page_table, T,
+                               storage_block_size=128, compress_ratio=4,
+                               common_slot_mapping=common, num_mapped_tokens=T, out=meta,
+                               stream=stream)
+        qsa.qsa_decode(w.q_sel, w.cmp_cache, w.cmp_page_table, meta["token_to_req"],
+                       w.seq_lens, meta["logical_positions"], w.q_attn, w.k_view, w.v_view,
+                       w.kv_page_table, indices=idx, out=out, sel_workspace=sel_ws,
+                       att_workspace=att_ws, error_word=err, stream=stream)
+
+    K = max(1, min(args.steps, 200))
+    ms = _time_calls(step, K, stream, dev, world)
+    if int(err.item()) != 0:
+        raise SystemExit(f"bench.py: device error word {int(err.item())} (speculative decode)")
+    pos = meta["logical_positions"].cpu().numpy()
+    idx_h = idx.cpu().numpy()
+    row_sel = sum(select_bytes_per_row(131072, int(pos[r])) for r in range(T))
+    # each request's keys once: the floor when the rows of a request share
+    # one pass over its pages
+    uniq_sel = sum(select_bytes_per_row(131072, 131071) for _ in range(nreq))
+    att = sum(attend_bytes_per_row(idx_h[r]) for r in range(T))
+    del w, idx, out, sel_ws, att_ws
+    return {"workload": "R%d_%dreq_x4tok_L131072" % (T, nreq), "value": T * world / (ms * 1e-3),
+            "unit": "rows/s", "ms_per_step": ms, "steps": K,
+            "launches_per_step": 5,
+            "algorithmic_bytes_rows_separate": row_sel + att,
+            "algorithmic_bytes_keys_shared": uniq_sel + att,
+            "frac_of_peak_rows_separate": (row_sel + att) / (ms * 1e-3) / 1e9 / peak,
+            "frac_of_peak_keys_shared": (uniq_sel + att) / (ms * 1e-3) / 1e9 / peak}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -496,6 +595,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8-E4M3 compressed-cache measurement")
+    ap.add_argument("--no-spec", action="store_true",
+                    help="skip the speculative-decode (4 tokens per request) measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps are required")

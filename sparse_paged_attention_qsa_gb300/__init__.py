@@ -1,8 +1,9 @@
 """GB300 (sm_103a) QSA sparse decode path: paged top-512 block selection and
-FP16 sparse paged attention, as hand-written CUDA kernels behind the C ABI in
-include/qsa.h.  This package is the Python binding (ctypes, marshalling
+FP16 sparse paged attention, plus the side-cache metadata builder that feeds
+them, as hand-written CUDA kernels behind the C ABI in include/qsa.h and
+include/qsa_metadata.h.  This package is the Python binding (ctypes, marshalling
 only), the in-tree build, and the seeded workload generators."""
 from .binding import (  # noqa: F401
     COMPRESS_RATIO, DERR_CMP_PAGE, DERR_KV_PAGE, DERR_REQUEST, EXPORTED, LIB_PATH,
     OUT_WIDTH, TOKEN_TOPK, TOPK_BLOCKS, QSAError, load_library, qsa_attention_workspace_bytes,
-    qsa_decode, qsa_select_paged_tokens, qsa_select_workspace_bytes, qsa_sparse_attention)
+    qsa_build_metadata, qsa_decode, qsa_select_paged_tokens, qsa_select_workspace_bytes, qsa_sparse_attention)

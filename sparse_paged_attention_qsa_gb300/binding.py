@@ -37,7 +37,7 @@ STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE"
 EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
             "qsa_sparse_attention", "qsa_static_scratch_bytes",
-            "qsa_select_paged_tokens_static_scratch")
+            "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata")
 
 
 class QSAError(RuntimeError):
@@ -92,6 +92,12 @@ def load_library(path: str | None = None):
             ctypes.c_float,
             vp, ctypes.c_int, p64,
             vp, sz, vp, vp]
+        lib.qsa_build_metadata.restype = ctypes.c_int
+        lib.qsa_build_metadata.argtypes = [
+            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+            vp, ctypes.c_int, i64, i64, i64, i64,
+            i64, i64, i64, i64, i64, i64,
+            vp, vp, vp, vp, vp, i64, vp]
         _lib = lib
         return lib
 
@@ -221,3 +227,56 @@ def qsa_decode(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens, que
                                indices, scale=scale, out=out, workspace=att_workspace,
                                error_word=error_word, stream=stream)
     return indices, out
+
+
+def qsa_build_metadata(query_start_loc, seq_lens, block_table, num_tokens: int, *,
+                       storage_block_size: int, compress_ratio: int,
+                       circular_buffer_size: int = 0, common_slot_mapping=None,
+                       num_mapped_tokens: int | None = None, max_num_work: int = 0,
+                       out=None, stream=None):
+    """Side-cache metadata (include/qsa_metadata.h).  Returns a dict of
+    device tensors: token_to_req int32, logical_positions int64,
+    visible_blocks int32, slot_mapping int64 (each [num_tokens]) and, when
+    max_num_work > 0, work_metadata int32 [max_num_work, 2].
+
+    ``num_mapped_tokens`` is the host's copy of query_start_loc[-1]; when it
+    is not given it is read from the device (one synchronising read).
+    ``out`` may hold preallocated tensors under the same keys."""
+    lib = load_library()
+    dev = query_start_loc.device
+    num_reqs = query_start_loc.numel() - 1
+    if query_start_loc.dim() != 1 or seq_lens.dim() != 1 or block_table.dim() != 2:
+        raise QSAError(3, "query_start_loc and seq_lens 1-D, block_table 2-D expected")
+    if not query_start_loc.is_contiguous() or not seq_lens.is_contiguous():
+        raise QSAError(4, "query_start_loc and seq_lens must be contiguous")
+    if seq_lens.numel() < num_reqs:
+        raise QSAError(3, "seq_lens shorter than the request count")
+    if num_mapped_tokens is None:
+        num_mapped_tokens = int(query_start_loc[-1].item())
+    out = dict(out or {})
+    T = int(num_tokens)
+    for key, dt in (("token_to_req", torch.int32), ("logical_positions", torch.int64),
+                    ("visible_blocks", torch.int32), ("slot_mapping", torch.int64)):
+        if key not in out:
+            out[key] = torch.empty(T, dtype=dt, device=dev)
+    if max_num_work and "work_metadata" not in out:
+        out["work_metadata"] = torch.empty((max_num_work, 2), dtype=torch.int32, device=dev)
+    work = out.get("work_metadata")
+    for key in ("token_to_req", "logical_positions", "visible_blocks", "slot_mapping"):
+        if out[key].numel() < T or not out[key].is_contiguous():
+            raise QSAError(3, f"{key} must be a contiguous tensor of >= num_tokens entries")
+    if work is not None and (not work.is_contiguous() or work.numel() < 2 * max_num_work):
+        raise QSAError(3, "work_metadata must be contiguous [max_num_work, 2]")
+    common = common_slot_mapping
+    st = lib.qsa_build_metadata(
+        _ptr(query_start_loc), _tag(query_start_loc), _ptr(seq_lens), _tag(seq_lens),
+        _ptr(common), _tag(common) if common is not None else 0,
+        _ptr(block_table), _tag(block_table), block_table.shape[0], block_table.shape[1],
+        block_table.stride(0), block_table.stride(1),
+        num_reqs, int(num_mapped_tokens), T,
+        int(storage_block_size), int(compress_ratio), int(circular_buffer_size),
+        _ptr(out["token_to_req"]), _ptr(out["logical_positions"]),
+        _ptr(out["visible_blocks"]), _ptr(out["slot_mapping"]),
+        _ptr(work) if max_num_work else None, int(max_num_work), _stream(stream))
+    _check(st)
+    return out

@@ -17,6 +17,10 @@ Layouts follow "vLLM: integrate FP16 packed QSA extension", "Exact contracts":
   page tables int32 [num_reqs, cols] (-1 = unused column)
   token_to_request int32 [R], seq_lens int32 [num_reqs],
   query_positions int64 [R]
+  query_start_loc int32 [num_reqs+1] (batches with several query tokens per
+                  request: request i owns rows query_start_loc[i] ..
+                  query_start_loc[i+1]-1; its token_to_request and
+                  query_positions are then left to the metadata builder)
 
 Structure (sequence lengths, page tables, premade index lists) is drawn from
 a CPU generator seeded with ``seed``; values (queries, keys, K/V) from a
@@ -45,14 +49,15 @@ class Workload:
     q_sel: torch.Tensor
     cmp_cache: torch.Tensor
     cmp_page_table: torch.Tensor
-    token_to_request: torch.Tensor
+    token_to_request: torch.Tensor | None
     seq_lens: torch.Tensor
-    query_positions: torch.Tensor
+    query_positions: torch.Tensor | None
     q_attn: torch.Tensor
     kv_cache: torch.Tensor
     kv_page_table: torch.Tensor
     indices: torch.Tensor | None = None    # premade attention index lists
     meta: dict = field(default_factory=dict)
+    query_start_loc: torch.Tensor | None = None   # multi-token batches
 
     @property
     def k_view(self) -> torch.Tensor:
@@ -101,8 +106,15 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
           cmp_std: float = 0.1, distinct_keys: int = 0,
           dup_mapping: bool = False, premade_widths: list[int] | None = None,
           hole_frac: float = 0.10, dup_frac: float = 0.05,
-          cmp_dtype: str = "fp16", seed: int = 0, device="cpu") -> Workload:
+          cmp_dtype: str = "fp16", query_lens: list[int] | None = None,
+          seed: int = 0, device="cpu") -> Workload:
     """General builder: one request per row (token_to_request = arange(R)).
+
+    ``query_lens`` instead gives request i query_lens[i] consecutive rows
+    (speculative / multi-token decode and prefill chunks; 0 = a request with
+    no rows): R = sum(query_lens), ``query_start_loc`` is their running sum,
+    and token_to_request / query_positions stay None for the metadata
+    builder to fill.
 
     ``positions`` default to seq_len-1 (plain decode).  Each request gets the
     compressed pages its seq_len needs (seq_len // 4 keys, 128 per page) and
@@ -121,9 +133,15 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
     if cmp_dtype not in ("fp16", "fp8"):
         raise ValueError("cmp_dtype must be 'fp16' or 'fp8'")
     kdt = torch.float8_e4m3fn if cmp_dtype == "fp8" else torch.float16
-    R = len(seq_lens)
+    nreq = len(seq_lens)
+    if query_lens is not None:
+        if len(query_lens) != nreq or positions is not None or premade_widths:
+            raise ValueError("query_lens: one per request, no positions / premade lists")
+        R = int(sum(query_lens))
+    else:
+        R = nreq
     sg = torch.Generator().manual_seed(seed)
-    if positions is None:
+    if positions is None and query_lens is None:
         positions = [L - 1 for L in seq_lens]
     cmp_need = [_pages_for(max(L, 0) // 4, CMP_PAGE) for L in seq_lens]
     kv_need = [_pages_for(max(L, 0), KV_PAGE) for L in seq_lens]
@@ -137,7 +155,7 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
 
     def tables(need, pool, cols):
         perm = torch.randperm(pool, generator=sg).tolist()
-        pt = torch.full((R, cols), -1, dtype=torch.int32)
+        pt = torch.full((nreq, cols), -1, dtype=torch.int32)
         at = 0
         for r, n in enumerate(need):
             if n:
@@ -147,7 +165,7 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
 
     cmp_pt = tables(cmp_need, cmp_pool, cmp_cols)
     kv_pt = tables(kv_need, kv_pool, kv_cols)
-    if dup_mapping and R >= 2:
+    if dup_mapping and nreq >= 2:
         for pt, need in ((cmp_pt, cmp_need), (kv_pt, kv_need)):
             if need[0] >= 2:
                 pt[0, 1] = pt[0, 0]              # request 0: one page, two columns
@@ -190,15 +208,22 @@ def build(name: str, seq_lens: list[int], *, positions: list[int] | None = None,
     q_attn = _fill_normal((R, ATT_HEADS, ATT_DIM), 1.0, vg, device)
     kv = _fill_normal((kv_pool, KV_PAGE, 2, ATT_DIM), 1.0, vg, device)
 
+    qsl = None
+    if query_lens is not None:
+        qsl = torch.zeros(nreq + 1, dtype=torch.int32)
+        qsl[1:] = torch.tensor(query_lens, dtype=torch.int32).cumsum(0)
     return Workload(
         name=name, R=R, q_sel=q_sel, cmp_cache=cmp,
         cmp_page_table=cmp_pt.to(device),
-        token_to_request=torch.arange(R, dtype=torch.int32).to(device),
+        token_to_request=None if qsl is not None else
+        torch.arange(R, dtype=torch.int32).to(device),
         seq_lens=torch.tensor(seq_lens, dtype=torch.int32).to(device),
-        query_positions=torch.tensor(positions, dtype=torch.int64).to(device),
+        query_positions=None if qsl is not None else
+        torch.tensor(positions, dtype=torch.int64).to(device),
         q_attn=q_attn, kv_cache=kv, kv_page_table=kv_pt.to(device),
         indices=indices.to(device) if indices is not None else None,
-        meta={"seed": seed, "cmp_pool": cmp_pool, "kv_pool": kv_pool})
+        meta={"seed": seed, "cmp_pool": cmp_pool, "kv_pool": kv_pool},
+        query_start_loc=qsl.to(device) if qsl is not None else None)
 
 
 # --- the five named workloads ------------------------------------------------

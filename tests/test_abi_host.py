@@ -1,10 +1,11 @@
 """Host-side checks of the C ABI (no GPU needed): the library loads, exports
-every function include/qsa.h declares, answers workspace queries, and fails
+every function include/*.h declares, answers workspace queries, and fails
 closed on bad arguments -- each rejected before any CUDA call, so fake
 (aligned, never dereferenced) device addresses are enough here.  Mirrors the
 fail-closed dtype/layout/output checks of "vLLM: integrate FP16 packed QSA
 extension" (Validation)."""
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -14,7 +15,8 @@ import pytest
 import sparse_paged_attention_qsa_gb300 as qsa
 from sparse_paged_attention_qsa_gb300 import build as qbuild
 
-HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qsa.h")
+INC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HDR = os.path.join(INC, "qsa.h")
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +26,7 @@ def lib():
 
 
 def _declared():
-    src = open(HDR).read()
+    src = "".join(open(h).read() for h in sorted(glob.glob(os.path.join(INC, "*.h"))))
     return re.findall(r"QSA_API\s+[\w\s\*]+?\b(qsa_\w+)\s*\(", src)
 
 
@@ -177,3 +179,44 @@ def test_binding_raises_without_library(tmp_path):
             b.load_library(str(tmp_path / "missing.so"))
     finally:
         b._lib = saved
+
+
+# --- fail-closed metadata builder -------------------------------------------
+
+def _meta(lib, **over):
+    T = over.pop("T", 300)
+    a = dict(qsl=_addr(1), qsldt=4, sl=_addr(2), sldt=4, common=_addr(3), cdt=5,
+             bt=_addr(4), btdt=4, rows=8, cols=16, s0=16, s1=1,
+             nreq=8, nmapped=T, T=T, sbs=128, cr=4, cbs=0,
+             t2r=_addr(10), lpos=_addr(11), vis=_addr(12), slot=_addr(13),
+             work=_addr(14), maxw=64, stream=None)
+    a.update(over)
+    return lib.qsa_build_metadata(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qsldt=5), 2), (dict(sldt=5), 2), (dict(btdt=5), 2), (dict(cdt=4), 2),
+    (dict(nreq=0), 3), (dict(T=-1), 3), (dict(T=1 << 31), 3), (dict(nmapped=-1), 3),
+    (dict(maxw=-1), 3), (dict(rows=7), 3), (dict(cols=-1), 3),
+    (dict(sbs=0), 6), (dict(cr=0), 6), (dict(cbs=-1), 6), (dict(cr=1 << 31), 6),
+    (dict(s0=0), 4), (dict(s1=0), 4),
+    (dict(qsl=None), 1), (dict(sl=None), 1), (dict(t2r=None), 1), (dict(lpos=None), 1),
+    (dict(vis=None), 1), (dict(slot=None), 1), (dict(bt=None), 1), (dict(common=None), 1),
+    (dict(work=None), 1),
+    (dict(qsl=_addr(1) + 2), 5), (dict(lpos=_addr(11) + 4), 5), (dict(slot=_addr(13) + 4), 5),
+    (dict(common=_addr(3) + 4), 5), (dict(work=_addr(14) + 2), 5),
+    (dict(t2r=_addr(11)), 8), (dict(slot=_addr(3)), 8), (dict(vis=_addr(10) + 1024), 8),
+    (dict(work=_addr(4)), 8), (dict(lpos=_addr(1)), 8),
+])
+def test_metadata_fails_closed(lib, over, status):
+    assert _meta(lib, **over) == status
+
+
+def test_metadata_nothing_to_do_and_optional_inputs(lib):
+    assert _meta(lib, T=0, maxw=0, work=None) == 0
+    # circular mode ignores common_slot_mapping (and its dtype tag)
+    assert _meta(lib, T=0, maxw=0, work=None, cbs=8, common=None, cdt=0) == 0
+    # a table without columns needs no pointer; no tokens need no outputs
+    assert _meta(lib, T=0, maxw=0, work=None, cols=0, bt=None) == 0
+    assert _meta(lib, T=0, maxw=0, work=None, t2r=None, lpos=None, vis=None, slot=None,
+                 common=None) == 0
