@@ -46,15 +46,19 @@ struct KeyCfg {
   static constexpr int kStages = kRingBytes / kPageBytes;
   static constexpr int kRowsPerKey = kFp8 ? 1 : 2;            // 128-byte TMA rows per key
 };
-#ifndef QSA_SCORE_WARPS
-#define QSA_SCORE_WARPS 8
-#endif
-constexpr int kScoreWarps = QSA_SCORE_WARPS;            // consumer warps: 8 or 16
+constexpr int kScoreWarps = 8;                          // consumer warps
 constexpr int kScoreThreads = (kScoreWarps + 1) * 32;   // + one producer warp
-constexpr int kScoreGroups = 16 / kScoreWarps;          // groups of 8 keys per warp per page
-constexpr int kMaxRows = 2048;                          // rows per launch (row tables in smem)
+constexpr int kKeyGroups = kCmpPageKeys / 8;            // groups of 8 keys per page
+static_assert(2 * kScoreWarps == kKeyGroups, "each consumer warp takes whole key-group pairs");
+constexpr int kMaxRows = 1024;                          // rows per launch (row tables in smem)
+constexpr int kGroupRows = 8;    // rows of one request scored from one page pass (aligned windows)
+// row tables: req, visible blocks; group tables: first row (+ sentinel), pages,
+// weighted page prefix (64-bit, + total)
+constexpr size_t kTableBytes = (size_t)(4 * kMaxRows + 1) * sizeof(int) +
+                               (size_t)(kMaxRows + 1) * sizeof(int64_t);
 constexpr size_t kScoreSmem = (size_t)kRingBytes + 1024 + 2 * kMaxStages * 8 +
-                              kMaxStages * 16 + 3 * kMaxRows * sizeof(int);
+                              kMaxStages * 16 + kTableBytes;
+static_assert(kScoreSmem <= 227 * 1024 - 256, "score kernel shared memory");
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s: any wait longer is a fault
 
 constexpr int kTopkThreads = 512;                       // one key per thread in the sort
@@ -212,27 +216,96 @@ __device__ __forceinline__ uint32_t quad_score(const uint32_t (&q)[kSelHeads][16
   return __float_as_uint(s) + 1u;
 }
 
+// This lane's query slice [32t, 32t+32) of each of the 4 heads, fp16 pairs.
+__device__ __forceinline__ void load_query_slice(const __half* qrow, int t,
+                                                 uint32_t (&q)[kSelHeads][16]) {
+  const uint4* qp = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll
+  for (int h = 0; h < kSelHeads; ++h) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(qp + h * 16 + t * 4 + i);
+      q[h][4 * i + 0] = v.x;
+      q[h][4 * i + 1] = v.y;
+      q[h][4 * i + 2] = v.z;
+      q[h][4 * i + 3] = v.w;
+    }
+  }
+}
+
+// Load NG consecutive groups of 8 keys (from group g0) of the staged page:
+// this lane's 32-dim slice of key (g0+g)*8 + kslot, as fp16 pairs.  With the
+// 128-byte swizzle, lane (key k, slice t) of an fp16 page reads row 2k + t/2,
+// 16-byte chunks (4(t&1)+j) XOR (row & 7); of an E4M3 page, row k, chunks
+// (2t+j) XOR (k & 7): the 8 lanes of each shared-memory phase hit 8 distinct
+// bank groups.
+template <bool kFp8, int NG>
+__device__ __forceinline__ void load_key_groups(uint32_t stage, int g0, int t, int kslot,
+                                                uint4 (&kv)[NG][4]) {
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int k = (g0 + g) * 8 + kslot;
+    if (kFp8) {
+      const uint32_t r = (uint32_t)k;
+      const uint32_t rbase = stage + r * 128;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t chunk = (uint32_t)(2 * t + j) ^ (r & 7u);
+        const uint4 c = lds128(rbase + chunk * 16);
+        e4m3x16_to_h(c, kv[g][2 * j], kv[g][2 * j + 1]);
+      }
+    } else {
+      const uint32_t r = 2 * k + (t >> 1);
+      const uint32_t rbase = stage + r * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (r & 7u);
+        kv[g][j] = lds128(rbase + chunk * 16);
+      }
+    }
+  }
+}
+
 struct StageDesc {
-  int row;        // -1: no more work
+  int row;        // first row of the group; -1: no more work
   int b0;         // first block of the page
-  int nkeys;      // visible keys in the page (<= 128)
+  int nrows;      // rows of the group (each scores its own visible keys)
   int pad;
 };
 
+// Work weight of one page for a group of n rows: a page costs at least its
+// stream time (about three rows' worth of fp16 scoring; one row for E4M3
+// pages, where scoring alone sets the pace), else the scoring of n rows.
+template <bool kFp8>
+__device__ __forceinline__ int page_cost(int n) {
+  constexpr int kFloor = kFp8 ? 1 : 3;
+  return n > kFloor ? n : kFloor;
+}
+
 // Persistent streaming score kernel over rows [0, p.R) (p.R <= kMaxRows).
 //
-// Prologue: every CTA computes each row's visible-page count and their
-// prefix sum in shared memory, so the W = sum of pages can be cut into
-// equal contiguous ranges, one per CTA (pages of one row are consecutive,
-// so a CTA changes rows rarely and reads consecutive page-table entries).
+// Row groups: consecutive rows of one request inside an aligned window of
+// kGroupRows rows (a request's speculative / multi-token query rows) read
+// the same compressed pages, so each page is streamed once per group and
+// scored for every row of the group (each row up to its own visible block
+// count).  A plain decode batch has one row per group.
+//
+// Prologue: every CTA computes the row and group tables in shared memory --
+// each row's request and visible blocks, each group's first row and page
+// count (the most any of its rows sees), and the prefix sum of the groups'
+// weighted page counts (page_cost) -- so the total work can be cut into
+// equal contiguous ranges, one per CTA (a CTA changes groups rarely and
+// reads consecutive page-table entries).
 //
 // Main loop, warp-specialised: lane 0 of the producer warp walks the CTA's
 // range and streams each page (32 KiB = 128 keys x two 128-byte rows) into a
 // ring of shared-memory stages with one 2-D TMA load (128-byte swizzle, L2
-// evict-first), writing a small stage descriptor (row, first block, key
-// count) before arming the stage; it refills a stage as soon as every
-// consumer warp has released it.  Each consumer warp scores 128/kScoreWarps
-// keys of every page.  With the swizzle, lane (key k, slice t) reads row
+// evict-first), writing a small stage descriptor (group's first row, first
+// block, rows) before arming the stage; it refills a stage as soon as every
+// consumer warp has released it.  The page's n rows x 16 groups of 8 keys
+// are split evenly over the 8 consumer warps (2n consecutive units each,
+// row-major, taken in pairs of one row), so for n = 1, 2, 4 or 8 a warp keeps
+// one row -- and its query slice in registers -- for all of a group's pages.  With the swizzle, lane (key k, slice t) reads row
 // 2k + t/2, 16-byte chunks (4(t&1)+j) XOR (row & 7): the 8 lanes of each
 // shared-memory phase hit 8 distinct bank groups, and each lane reads its
 // slice in ascending order.
@@ -244,7 +317,8 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ int s_abort;
   __shared__ int64_t s_total;
-  __shared__ int warp_sum[kScoreWarps];
+  __shared__ int s_ngroups;
+  __shared__ int64_t warp_sum[kScoreWarps];
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   const uint32_t base = raw + pad;
@@ -252,9 +326,11 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   const uint32_t bar_empty = bar_full + kMaxStages * 8;
   unsigned char* gbase = smem_raw + pad;
   StageDesc* desc = reinterpret_cast<StageDesc*>(gbase + kRingBytes + 2 * kMaxStages * 8);
-  int* row_req = reinterpret_cast<int*>(desc + kMaxStages);
+  int64_t* grp_pre = reinterpret_cast<int64_t*>(desc + kMaxStages);  // weighted prefix [NG+1]
+  int* row_req = reinterpret_cast<int*>(grp_pre + kMaxRows + 1);
   int* row_vs = row_req + kMaxRows;
-  int* row_pre = row_vs + kMaxRows;          // exclusive prefix of page counts
+  int* grp_first = row_vs + kMaxRows;        // [NG+1], sentinel p.R
+  int* grp_pages = grp_first + kMaxRows + 1;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -271,47 +347,92 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
 
-  // ---- prologue (consumer threads): per-row visible pages, prefix sum ----
+  // ---- prologue (consumer threads): row and group tables ----
   constexpr int kConsumerThreads = kScoreWarps * 32;
   constexpr int kRowsPerThread = kMaxRows / kConsumerThreads;
+  static_assert(kMaxRows % kConsumerThreads == 0, "rows per consumer thread");
   if (!is_producer_warp) {
-    int cnt[kRowsPerThread];
-    int mine = 0;
+    const auto consumers_sync = [] {
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumerThreads) : "memory");
+    };
+    // block-wide exclusive scan over the consumer threads (int64)
+    const auto scan = [&](int64_t mine, int64_t& total) -> int64_t {
+      int64_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) warp_sum[warp] = incl;
+      consumers_sync();
+      int64_t before = 0;
+      total = 0;
+      for (int w = 0; w < kScoreWarps; ++w) {
+        before += (w < warp) ? warp_sum[w] : 0;
+        total += warp_sum[w];
+      }
+      consumers_sync();                     // warp_sum is reused by the next scan
+      return before + incl - mine;
+    };
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
       const int r = tid * kRowsPerThread + i;
-      cnt[i] = 0;
       if (r < p.R) {
         const RowSetup rs = row_setup(p, r);
         const int64_t Vs = rs.ok ? (rs.V < p.vcap ? rs.V : p.vcap) : 0;
         row_req[r] = rs.ok ? rs.req : -1;
         row_vs[r] = (int)Vs;
-        cnt[i] = (int)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
       }
-      mine += cnt[i];
     }
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerThreads) : "memory");
-    int before = 0;
-    int64_t tot = 0;
-    for (int w = 0; w < kScoreWarps; ++w) {
-      before += (w < warp) ? warp_sum[w] : 0;
-      tot += warp_sum[w];
-    }
-    int run = before + incl - mine;
+    consumers_sync();
+    // group starts: window boundary, request change, or a row without a request
+    int starts = 0, nstart = 0;
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
       const int r = tid * kRowsPerThread + i;
-      if (r < p.R) row_pre[r] = run;
-      run += cnt[i];
+      if (r < p.R) {
+        const bool st = (r % kGroupRows) == 0 || row_req[r] < 0 || row_req[r] != row_req[r - 1];
+        starts |= (int)st << i;
+        nstart += st;
+      }
     }
-    if (tid == 0) s_total = tot;
+    int64_t ngroups = 0;
+    int g = (int)scan(nstart, ngroups);
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i)
+      if (starts >> i & 1) grp_first[g++] = tid * kRowsPerThread + i;
+    if (tid == 0) grp_first[ngroups] = p.R;
+    consumers_sync();
+    // per group: pages (the most any of its rows sees) and weighted pages
+    int64_t wsum = 0;
+    int64_t wg[kRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int gi = tid * kRowsPerThread + i;
+      wg[i] = 0;
+      if (gi < ngroups) {
+        const int f = grp_first[gi], l = grp_first[gi + 1];
+        int vmax = 0;
+        for (int r = f; r < l; ++r) vmax = row_vs[r] > vmax ? row_vs[r] : vmax;
+        const int pages = (vmax + kCmpPageKeys - 1) / kCmpPageKeys;
+        grp_pages[gi] = pages;
+        wg[i] = (int64_t)pages * page_cost<kFp8>(l - f);
+      }
+      wsum += wg[i];
+    }
+    int64_t total = 0;
+    int64_t run = scan(wsum, total);
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int gi = tid * kRowsPerThread + i;
+      if (gi < ngroups) grp_pre[gi] = run;
+      run += wg[i];
+    }
+    if (tid == 0) {
+      grp_pre[ngroups] = total;
+      s_total = total;
+      s_ngroups = (int)ngroups;
+    }
   }
   __syncthreads();
 
@@ -325,16 +446,22 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
     // ---------------- producer (one lane) ----------------
     if (lane == 0) {
       const uint64_t policy = evict_first_policy();
-      int64_t pw = w_begin;
-      int prow = 0, pcol = 0;
-      if (pw < w_end) {   // row holding page pw: last r with row_pre[r] <= pw
-        int lo = 0, hi = p.R - 1;
+      const int NG = s_ngroups;
+      // first owned page: the first (group, page) whose weighted start is >= w_begin
+      int pgrp = NG, pcol = 0;
+      if (w_begin < w_end && NG > 0) {
+        int lo = 0, hi = NG - 1;             // last group with grp_pre <= w_begin
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (row_pre[mid] <= pw) lo = mid; else hi = mid - 1;
+          if (grp_pre[mid] <= w_begin) lo = mid; else hi = mid - 1;
         }
-        prow = lo;
-        pcol = (int)(pw - row_pre[prow]);
+        pgrp = lo;
+        const int64_t c = page_cost<kFp8>(grp_first[lo + 1] - grp_first[lo]);
+        pcol = (int)((w_begin - grp_pre[lo] + c - 1) / c);
+        while (pgrp < NG && pcol >= grp_pages[pgrp]) {
+          ++pgrp;
+          pcol = 0;
+        }
       }
       for (;;) {
         const int s = (int)(issued % kStages);
@@ -345,29 +472,30 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
           break;
         }
         if (*abort_flag) break;
-        // next page with a loadable physical page (zero-fill the others)
+        // next owned page with a loadable physical page (the others get no key)
         int32_t pg = -1;
-        while (pw < w_end) {
-          const int req = row_req[prow];
-          const int vs = row_vs[prow];
+        while (pgrp < NG) {
+          const int row0 = grp_first[pgrp];
+          const int n = grp_first[pgrp + 1] - row0;
+          if (grp_pre[pgrp] + (int64_t)pcol * page_cost<kFp8>(n) >= w_end) break;
           const int b0 = pcol * kCmpPageKeys;
-          pg = __ldg(p.pt + (int64_t)req * p.pt_stride0 + pcol);
-          const int nk = vs - b0 < kCmpPageKeys ? vs - b0 : kCmpPageKeys;
-          const int row = prow;
-          ++pw;
-          if (++pcol * kCmpPageKeys >= vs) {
+          pg = __ldg(p.pt + (int64_t)row_req[row0] * p.pt_stride0 + pcol);
+          if (++pcol >= grp_pages[pgrp]) {
             pcol = 0;
-            ++prow;
-            while (prow < p.R && row_vs[prow] == 0) ++prow;
+            ++pgrp;
+            while (pgrp < NG && grp_pages[pgrp] == 0) ++pgrp;
           }
           if (pg >= 0 && pg < p.num_pages) {
-            desc[s].row = row;
+            desc[s].row = row0;
             desc[s].b0 = b0;
-            desc[s].nkeys = nk;
+            desc[s].nrows = n;
             break;
           }
-          uint32_t* zr = p.scores + (int64_t)row * p.vcap + b0;   // no key for these blocks
-          for (int k = 0; k < nk; ++k) zr[k] = 0u;
+          for (int j = 0; j < n; ++j) {          // no key for these blocks
+            const int nk = min(row_vs[row0 + j] - b0, kCmpPageKeys);
+            uint32_t* zr = p.scores + (int64_t)(row0 + j) * p.vcap + b0;
+            for (int k = 0; k < nk; ++k) zr[k] = 0u;
+          }
           report(p.err, kErrCmpPage);
           pg = -1;
         }
@@ -400,54 +528,28 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
       }
       const StageDesc d = desc[s];
       if (d.row < 0) break;
-      if (d.row != loaded_row) {
-        loaded_row = d.row;
-        srow = p.scores + (int64_t)d.row * p.vcap;
-        // query slice [32t, 32t+32) of each head, fp16 pairs
-        const uint4* qp = reinterpret_cast<const uint4*>(p.q_sel + (int64_t)d.row * kSelHeads * kSelDim);
-#pragma unroll
-        for (int h = 0; h < kSelHeads; ++h) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v = qp[h * 16 + t * 4 + i];
-            q[h][4 * i + 0] = v.x;
-            q[h][4 * i + 1] = v.y;
-            q[h][4 * i + 2] = v.z;
-            q[h][4 * i + 3] = v.w;
-          }
-        }
-      }
       const uint32_t stage = base + s * kPageBytes;
-      uint4 kv[kScoreGroups][4];
-#pragma unroll
-      for (int g = 0; g < kScoreGroups; ++g) {
-        const int k = (warp * kScoreGroups + g) * 8 + kslot;
-        if (kFp8) {
-          // one 128-byte row per key; slice t = 16-byte chunks 2t, 2t+1
-          const uint32_t row = (uint32_t)k;
-          const uint32_t rbase = stage + row * 128;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint32_t chunk = (uint32_t)(2 * t + j) ^ (row & 7u);
-            const uint4 c = lds128(rbase + chunk * 16);
-            e4m3x16_to_h(c, kv[g][2 * j], kv[g][2 * j + 1]);
-          }
-        } else {
-          // two 128-byte rows per key; slice t = row 2k + t/2, chunks 4(t&1)+j
-          const uint32_t row = 2 * k + (t >> 1);
-          const uint32_t rbase = stage + row * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t chunk = (uint32_t)(4 * (t & 1) + j) ^ (row & 7u);
-            kv[g][j] = lds128(rbase + chunk * 16);
-          }
+      // the page's n rows x 16 key groups, row-major, split evenly: this warp
+      // takes 2n consecutive units, in pairs of key groups of one row
+      const int units = 2 * d.nrows;
+      for (int u = warp * units; u < (warp + 1) * units; u += 2) {
+        const int row = d.row + u / kKeyGroups;
+        const int g0 = u % kKeyGroups;
+        uint4 kv[2][4];
+        load_key_groups<kFp8, 2>(stage, g0, t, kslot, kv);   // in flight while the row is checked
+        const int nk = row_vs[row] - d.b0;   // this row's visible keys in the page
+        if (nk <= 8 * g0) continue;          // both groups past the row's visible keys
+        if (row != loaded_row) {
+          loaded_row = row;
+          srow = p.scores + (int64_t)row * p.vcap;
+          load_query_slice(p.q_sel + (int64_t)row * kSelHeads * kSelDim, t, q);
         }
-      }
 #pragma unroll
-      for (int g = 0; g < kScoreGroups; ++g) {
-        const uint32_t key = quad_score(q, kv[g], t);
-        const int k = (warp * kScoreGroups + g) * 8 + kslot;
-        if (t == 0 && k < d.nkeys) srow[d.b0 + k] = key;
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t key = quad_score(q, kv[g], t);
+          const int k = (g0 + g) * 8 + kslot;
+          if (t == 0 && k < nk) srow[d.b0 + k] = key;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage

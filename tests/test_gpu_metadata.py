@@ -217,3 +217,55 @@ def test_mixed_prefill_chunk_and_decode_chain():
     ql = [40, 0, 1, 3, 5, 0]
     w = W.build("mixed", L, query_lens=ql, seed=72, device=DEV)
     _chain(w, rows_checked=[0, 1, 17, 38, 39, 40, 41, 42, 43, 44, 45, 46, 47, 48])
+
+
+def _with_positions(w):
+    m = M.build_metadata(w.query_start_loc.cpu().numpy(), w.seq_lens.cpu().numpy(),
+                         w.cmp_page_table.cpu().numpy(), w.R, storage_block_size=128,
+                         compress_ratio=4, common_slot_mapping=np.zeros(w.R, np.int64))
+    return W.Workload(**{**w.__dict__,
+                         "token_to_request": torch.from_numpy(m["token_to_req"]).to(DEV),
+                         "query_positions": torch.from_numpy(m["logical_positions"]).to(DEV)})
+
+
+def _select_parity(w, pt=None):
+    pt = w.cmp_page_table if pt is None else pt
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, pt, w.token_to_request,
+                                      w.seq_lens, w.query_positions, error_word=err)
+    torch.cuda.synchronize()
+    exp, oerr = oracle_select(w, cmp_page_table=pt)
+    g = got.cpu().numpy()
+    for r in range(w.R):
+        assert np.array_equal(g[r], exp[r]), r
+    assert int(err.item()) == oerr
+    return g
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_row_groups_straddling_pages_and_windows(fp8):
+    # rows of one request see different block counts: L = 517 gives 128, 128,
+    # 129, 129 visible blocks (1 or 2 pages); L = 2053 crosses the 512-block
+    # saturation; query lengths 3, 5, 7, 9 make groups break at the 8-row
+    # window edges
+    L = [517, 2053, 700, 30000, 131, 5000, 9000]
+    ql = [4, 4, 3, 5, 7, 9, 1]
+    w = _with_positions(W.build("groups", L, query_lens=ql, cmp_dtype="fp8" if fp8 else "fp16",
+                                seed=80, device=DEV))
+    _select_parity(w)
+
+
+def test_row_groups_bad_page_inside_group():
+    L = [3000, 6000, 1000]
+    w = _with_positions(W.build("groupbad", L, query_lens=[4, 6, 2], seed=81, device=DEV))
+    pt = w.cmp_page_table.clone()
+    pt[1, 3] = -5                           # a missing page inside request 1's rows
+    pt[0, 0] = w.cmp_cache.shape[0] + 1     # and past the pool for request 0
+    g = _select_parity(w, pt)
+    assert (g[:4] >= 0).sum() > 0
+
+
+def test_row_groups_ties_and_duplicate_pages():
+    w = _with_positions(W.build("groupties", [6003, 4099, 30001], query_lens=[4, 4, 8],
+                                distinct_keys=4, dup_mapping=True, seed=82, device=DEV))
+    _select_parity(w)
