@@ -395,6 +395,9 @@ def run_ours(args, world, rank, local):
     spec = None
     if not args.no_spec and args.workload == 4:
         spec = spec_variant(args, R, world, rank, dev, stream, peak)
+    indexer = None
+    if not args.no_indexer and args.workload == 4:
+        indexer = indexer_variant(args, world, rank, dev, stream, peak)
     sel_gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
     att_gbs = att_bytes / (att_ms * 1e-3) / 1e9
     step_gbs = (sel_bytes + att_bytes) / (total_ms / K * 1e-3) / 1e9
@@ -436,6 +439,7 @@ def run_ours(args, world, rank, local):
         "fp8_compressed_cache": fp8,
         "metadata_builder": meta,
         "speculative_decode": spec,
+        "paged_mqa_indexer": indexer,
         "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
@@ -582,6 +586,65 @@ def spec_variant(args, R, world, rank, dev, stream, peak):
             "frac_of_peak_keys_shared": (uniq_sel + att) / (ms * 1e-3) / 1e9 / peak}
 
 
+def indexer_variant(args, world, rank, dev, stream, peak):
+    """The weighted paged MQA indexer decode step (DeepSeek-V3.2 style):
+    128 requests x 2 query tokens x 64 heads over 65536 cached tokens each
+    (block size 64), FP8 tensor-core logits then the per-row top-2048.
+    Inputs resident (1.1 GB of cache); each step streams the whole cache."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    B, next_n, H, ctx, topk = 128, 2, 64, 65536, 2048
+    ib = W.indexer_batch("indexer_B128_n2_H64_L65536", [ctx] * B, next_n=next_n, heads=H,
+                         block_size=64, max_model_len=ctx, extra_blocks=0,
+                         seed=777 + 7919 * rank, device=dev)
+    rows = B * next_n
+    logits = torch.empty((rows, ctx), dtype=torch.float32, device=dev)
+    idx = torch.empty((rows, topk), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def lg():
+        qsa.qsa_paged_mqa_logits(ib.q, ib.kv_cache, ib.weights, ib.context_lens,
+                                 ib.block_tables, next_n, ctx, block_size=64, out=logits,
+                                 error_word=err, stream=stream)
+
+    def tk():
+        qsa.qsa_top_k_per_row_decode(logits, next_n, ib.context_lens, topk, out=idx,
+                                     stream=stream)
+
+    for _ in range(args.warmup):
+        lg()
+        tk()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise SystemExit(f"bench.py: device error word {int(err.item())} (indexer)")
+    K = max(1, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    for i in range(K):
+        ev[i][0].record(stream)
+        lg()
+        ev[i][1].record(stream)
+        tk()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    lg_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    tk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world, dev)
+    cache_bytes = B * ctx * 132
+    lg_bytes = cache_bytes + rows * H * (128 + 4) + rows * ctx * 4 + B * 4 + B * (ctx // 64) * 4
+    tk_bytes = rows * ctx * 4 + rows * topk * 4 + B * 4
+    flops = 2.0 * rows * ctx * H * 128
+    gbs = lg_bytes / (lg_ms * 1e-3) / 1e9
+    del ib, logits, idx
+    return {"workload": "B128_nextn2_H64_L65536_bs64_top2048", "value": rows * world / (step * 1e-3),
+            "unit": "rows/s", "ms_per_step": step, "steps": K, "logits_ms": lg_ms,
+            "topk_ms": tk_ms, "logits_algorithmic_bytes": lg_bytes, "logits_hbm_gbs": gbs,
+            "logits_frac_of_peak": gbs / peak, "logits_fp8_tflops": flops / (lg_ms * 1e-3) / 1e12,
+            "topk_algorithmic_bytes": tk_bytes,
+            "topk_gbs": tk_bytes / (tk_ms * 1e-3) / 1e9, "launches_per_step": 3}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -597,6 +660,8 @@ def main():
                     help="skip the FP8-E4M3 compressed-cache measurement")
     ap.add_argument("--no-spec", action="store_true",
                     help="skip the speculative-decode (4 tokens per request) measurement")
+    ap.add_argument("--no-indexer", action="store_true",
+                    help="skip the paged MQA indexer measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps are required")

@@ -24,6 +24,8 @@ COMPRESS_RATIO = 4
 TOPK_BLOCKS = 512
 OUT_WIDTH = 2051
 DERR_REQUEST, DERR_CMP_PAGE, DERR_KV_PAGE, DERR_TIMEOUT = 1, 2, 4, 8
+DERR_IDX_BLOCK = 16
+IDX_HEAD_DIM, IDX_MAX_TOPK = 128, 2048
 
 DT_F16, DT_BF16, DT_F32, DT_I32, DT_I64, DT_F8E4M3 = 1, 2, 3, 4, 5, 6
 _DTYPE_TAG = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_F32,
@@ -37,7 +39,8 @@ STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE"
 EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
             "qsa_sparse_attention", "qsa_static_scratch_bytes",
-            "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata")
+            "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata",
+            "qsa_paged_mqa_logits", "qsa_top_k_per_row_decode")
 
 
 class QSAError(RuntimeError):
@@ -98,6 +101,21 @@ def load_library(path: str | None = None):
             vp, ctypes.c_int, i64, i64, i64, i64,
             i64, i64, i64, i64, i64, i64,
             vp, vp, vp, vp, vp, i64, vp]
+        lib.qsa_paged_mqa_logits.restype = ctypes.c_int
+        lib.qsa_paged_mqa_logits.argtypes = [
+            vp, ctypes.c_int, i64, i64,
+            vp, ctypes.c_int, i64, i64,
+            vp, ctypes.c_int,
+            vp, ctypes.c_int, i64,
+            vp, ctypes.c_int, i64, i64,
+            i64,
+            vp, ctypes.c_int, i64, i64,
+            vp, vp]
+        lib.qsa_top_k_per_row_decode.restype = ctypes.c_int
+        lib.qsa_top_k_per_row_decode.argtypes = [
+            vp, ctypes.c_int, i64, i64, i64, i64, i64,
+            vp, ctypes.c_int, i64,
+            i64, vp, ctypes.c_int, i64, vp]
         _lib = lib
         return lib
 
@@ -278,5 +296,61 @@ def qsa_build_metadata(query_start_loc, seq_lens, block_table, num_tokens: int, 
         _ptr(out["token_to_req"]), _ptr(out["logical_positions"]),
         _ptr(out["visible_blocks"]), _ptr(out["slot_mapping"]),
         _ptr(work) if max_num_work else None, int(max_num_work), _stream(stream))
+    _check(st)
+    return out
+
+
+def qsa_paged_mqa_logits(q, kv_cache, weights, context_lens, block_tables, next_n: int,
+                         max_model_len: int, *, block_size: int, out=None, error_word=None,
+                         stream=None):
+    """Weighted paged MQA indexer logits (include/qsa_indexer.h): returns fp32
+    [rows, max_model_len].  q is E4M3 [rows, heads, 128]; kv_cache holds
+    [num_blocks, block_size*132] bytes (uint8 or float8_e4m3fn storage)."""
+    lib = load_library()
+    if q.dim() != 3 or kv_cache.dim() != 2 or weights.dim() != 2 or block_tables.dim() != 2:
+        raise QSAError(3, "q [rows,H,128], kv_cache [blocks, bs*132], weights [rows,H], "
+                          "block_tables 2-D expected")
+    if not (q.is_contiguous() and kv_cache.is_contiguous() and weights.is_contiguous()
+            and context_lens.is_contiguous()):
+        raise QSAError(4, "q, kv_cache, weights and context_lens must be contiguous")
+    if kv_cache.shape[1] != block_size * (IDX_HEAD_DIM + 4):
+        raise QSAError(3, "kv_cache rows must hold block_size * 132 bytes")
+    if block_tables.shape[1] > 1 and block_tables.stride(1) != 1:
+        raise QSAError(4, "block-table columns must be contiguous")
+    rows, heads = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((rows, max_model_len), dtype=torch.float32, device=q.device)
+    if out.dim() != 2 or (out.shape[1] > 1 and out.stride(1) != 1):
+        raise QSAError(4, "logits must be 2-D with contiguous columns")
+    kv_tag = DT_F8E4M3 if kv_cache.dtype in (torch.uint8, torch.float8_e4m3fn) else 0
+    st = lib.qsa_paged_mqa_logits(
+        _ptr(q), _tag(q), rows, heads,
+        _ptr(kv_cache), kv_tag, kv_cache.shape[0], int(block_size),
+        _ptr(weights), _tag(weights),
+        _ptr(context_lens), _tag(context_lens), context_lens.numel(),
+        _ptr(block_tables), _tag(block_tables), block_tables.shape[1], block_tables.stride(0),
+        int(next_n),
+        _ptr(out), _tag(out), int(max_model_len), out.stride(0),
+        _ptr(error_word), _stream(stream))
+    _check(st)
+    return out
+
+
+def qsa_top_k_per_row_decode(logits, next_n: int, seq_lens, topk_tokens: int, out=None,
+                             stream=None):
+    """Per-row top-k of the indexer logits (include/qsa_indexer.h): returns
+    int32 [rows, topk_tokens], -1 padded."""
+    lib = load_library()
+    if logits.dim() != 2:
+        raise QSAError(3, "logits must be 2-D")
+    rows, cols = logits.shape
+    if out is None:
+        out = torch.empty((rows, topk_tokens), dtype=torch.int32, device=logits.device)
+    if out.dim() != 2 or (out.shape[1] > 1 and out.stride(1) != 1):
+        raise QSAError(4, "indices must be 2-D with contiguous columns")
+    st = lib.qsa_top_k_per_row_decode(
+        _ptr(logits), _tag(logits), rows, cols, logits.stride(0), logits.stride(1),
+        int(next_n), _ptr(seq_lens), _tag(seq_lens), seq_lens.numel(),
+        int(topk_tokens), _ptr(out), _tag(out), out.stride(0), _stream(stream))
     _check(st)
     return out

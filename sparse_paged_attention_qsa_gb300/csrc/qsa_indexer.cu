@@ -1,0 +1,810 @@
+// qsa_indexer.cu -- the weighted paged MQA indexer and its per-row top-k,
+// declared in include/qsa_indexer.h.
+//
+// "[XPU] Enable multiple key kernels for sparse attention" (vLLM PR 37888
+// report) names the DeepSeek-V3.2 indexer's decode kernels,
+// fp8_paged_mqa_logits and top_k_per_row_decode, and prints their
+// signatures; the arithmetic restated here is the plainest reading of them
+// (see the header): logit = key scale * sum_h w_h * ReLU(q_h . k).
+//
+// logits_kernel  persistent, one CTA per SM, warp-specialised:
+//   warp 0  producer: per 128-token tile of one request, TMA loads of the
+//           tile's cache blocks (128-byte value rows, 128-byte swizzle), the
+//           request's query rows (all heads of its next_n tokens, same
+//           swizzle), and plain bulk copies of the blocks' scales and the
+//           rows' head weights, into a ring of shared-memory stages;
+//   warp 1  one lane issues four tcgen05.mma kind::f8f6f4 (M = 128 tokens,
+//           N = next_n x heads, K = 32 each) per tile into one of two TMEM
+//           accumulators, then commits to the accumulator's and the stage's
+//           barriers; the warp owns the TMEM allocation;
+//   warps 2-5  epilogue: each thread owns one token (its TMEM lane), reads
+//           its accumulator row 16 columns at a time (tcgen05.ld), forms
+//           sum_h w_h * ReLU(d_h) per query row in fp32, scales, and writes
+//           the logits (consecutive threads, consecutive columns).
+// fill_kernel    writes -inf to each row's columns [L_r, max_model_len).
+// topk_rows_kernel  one CTA per row: exact radix select (11/11/10 bits) of
+//           the k-th largest ordered logit, emission of the larger ones and
+//           of the first ties in column order, bitonic sort of the k
+//           (logit, column) pairs.
+// Every mbarrier wait gives up after 1 s (QSA_DERR_TIMEOUT), drains what the
+// CTA has in flight, frees its TMEM and returns.
+#include "qsa.h"
+#include "qsa_indexer.h"
+#include "qsa_device.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+namespace qsa {
+namespace {
+
+constexpr int kDim = QSA_IDX_HEAD_DIM;      // 128 E4M3 values per query head / key
+constexpr int kTile = 128;                  // tokens per tile (MMA M)
+constexpr int kMaxN = 256;                  // next_n x heads (MMA N)
+constexpr int kLogitThreads = 6 * 32;
+constexpr int kMaxBatch = 1024;             // requests per launch (tables in smem)
+constexpr int kMaxStages = 8;
+constexpr size_t kLogitSmem = 220 * 1024;
+constexpr size_t kTablesBytes = (size_t)(kMaxBatch + 1) * 8 + (size_t)kMaxBatch * 4;
+constexpr size_t kMiscBytes = 1024;         // barriers + stage descriptors
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint32_t kErrTimeoutBit = 8u;
+constexpr uint32_t kErrBlockBit = QSA_DERR_IDX_BLOCK;
+
+struct LogitParams {
+  const uint8_t* kv;          // cache base [num_blocks, bs*132]
+  const float* w;             // this launch's first row's weights [rows, H]
+  const int32_t* ctx;         // this launch's requests' context lengths
+  const int32_t* bt;          // this launch's requests' block-table rows
+  int64_t num_blocks, bt_cols, bt_s0;
+  float* logits;              // this launch's first row
+  int64_t ld, max_len;
+  uint32_t* err;
+  int bs, H, next_n, N;
+  int batch;                  // requests in this launch
+  int qrow0;                  // query-map row of this launch's first request (b0 * N)
+  int stage_bytes, stages;
+  uint32_t tmem_cols;
+};
+
+struct TileDesc {
+  int b;          // request within the launch; -1: no more work
+  int tile;       // tile index within the request
+  uint32_t missing;  // bit c: block c of the tile had no valid cache block
+  int pad;
+};
+
+// --- PTX helpers -------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool try_wait(uint32_t a, uint32_t ph) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(a), "r"(ph) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_phase(uint32_t a, uint32_t ph) {
+  if (try_wait(a, ph)) return true;
+  const uint64_t t0 = gtime();
+  while (!try_wait(a, ph))
+    if (gtime() - t0 > kWaitNs) return false;
+  return true;
+}
+__device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x),
+      "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x),
+      "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// K-major operand, rows of 128 bytes, 128-byte swizzle, 8-row atoms 1024 B apart
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ int64_t row_len(int64_t ctx, int next_n, int j, int64_t max_len) {
+  int64_t L = ctx - next_n + j + 1;
+  L = L < max_len ? L : max_len;
+  return L > 0 ? L : 0;
+}
+
+// --- logits ------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kLogitThreads, 1)
+logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
+              const __grid_constant__ CUtensorMap qmap) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int64_t s_part[kLogitThreads];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  const uint32_t base = raw + pad;
+  unsigned char* gbase = smem_raw + pad;
+  const int S = p.stages;
+  const uint32_t misc = base + (uint32_t)(S * p.stage_bytes);
+  const uint32_t bar_full = misc, bar_empty = misc + 8 * kMaxStages;
+  const uint32_t bar_accf = misc + 16 * kMaxStages, bar_acce = bar_accf + 16;
+  TileDesc* desc = reinterpret_cast<TileDesc*>(gbase + S * p.stage_bytes + 16 * kMaxStages + 32);
+  int64_t* pre = reinterpret_cast<int64_t*>(gbase + S * p.stage_bytes + kMiscBytes);
+  int32_t* ctxc = reinterpret_cast<int32_t*>(pre + kMaxBatch + 1);
+  const int N = p.N;
+  const uint32_t kOff = 0, qOff = kTile * kDim, scOff = qOff + (uint32_t)N * kDim,
+                 wOff = scOff + kTile * 4;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      bar_init(bar_full + 8 * s, 1);
+      bar_init(bar_empty + 8 * s, 1 + 4);    // MMA commit + 4 epilogue warps
+    }
+    for (int a = 0; a < 2; ++a) {
+      bar_init(bar_accf + 8 * a, 1);
+      bar_init(bar_acce + 8 * a, 4);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    const uint32_t slot = (uint32_t)__cvta_generic_to_shared(&s_tmem);
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // prologue: tiles per request and their prefix sum
+  for (int b = tid; b < p.batch; b += kLogitThreads) {
+    int64_t c = p.ctx[b];
+    c = c < p.max_len ? c : p.max_len;
+    ctxc[b] = (int32_t)(c > 0 ? c : 0);
+  }
+  __syncthreads();
+  {
+    const int per = (p.batch + kLogitThreads - 1) / kLogitThreads;
+    const int lo = tid * per, hi = min(p.batch, lo + per);
+    int64_t sum = 0;
+    for (int b = lo; b < hi; ++b) sum += (ctxc[b] + kTile - 1) / kTile;
+    s_part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t run = 0;
+      for (int i = 0; i < kLogitThreads; ++i) {
+        const int64_t v = s_part[i];
+        s_part[i] = run;
+        run += v;
+      }
+      pre[p.batch] = run;
+    }
+    __syncthreads();
+    int64_t run = s_part[tid];
+    for (int b = lo; b < hi; ++b) {
+      pre[b] = run;
+      run += (ctxc[b] + kTile - 1) / kTile;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int64_t W = pre[p.batch];
+  const int64_t w_begin = W * blockIdx.x / gridDim.x;
+  const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
+  volatile int* abort_flag = &s_abort;
+  int64_t issued = 0;    // producer: stages armed; MMA: tiles issued
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int b = 0;
+      int64_t i = 0;
+      if (w_begin < w_end) {
+        int lo = 0, hi = p.batch - 1;     // last request with pre <= w_begin
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pre[mid] <= w_begin) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        i = w_begin - pre[b];
+      }
+      int64_t w = w_begin;
+      const int blocks_per_tile = kTile / p.bs;
+      for (;; ++issued) {
+        const int s = (int)(issued % S);
+        if (issued >= S && !wait_phase(bar_empty + 8 * s, (uint32_t)(((issued / S) - 1) & 1))) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeoutBit);
+          break;
+        }
+        if (*abort_flag) break;
+        if (w >= w_end) {
+          desc[s].b = -1;
+          bar_arrive(bar_full + 8 * s);
+          ++issued;
+          break;
+        }
+        while (i >= (ctxc[b] + kTile - 1) / kTile) {   // skip requests without tiles
+          ++b;
+          i = 0;
+        }
+        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
+        const uint32_t full = bar_full + 8 * s;
+        const int64_t tv64 = ctxc[b] - i * kTile;
+        const int tv = (int)(tv64 < kTile ? tv64 : kTile);      // valid tokens in the tile
+        int nblk = (tv + p.bs - 1) / p.bs;
+        uint32_t missing = 0, bytes = (uint32_t)N * kDim + (uint32_t)N * 4;
+        int32_t blk_id[kTile / 8];
+        for (int c = 0; c < nblk; ++c) {
+          const int64_t col = i * blocks_per_tile + c;
+          const int32_t id = col < p.bt_cols ? __ldg(p.bt + (int64_t)b * p.bt_s0 + col) : -1;
+          blk_id[c] = id;
+          if (id < 0 || id >= p.num_blocks) {
+            missing |= 1u << c;
+            report(p.err, kErrBlockBit);
+          } else {
+            bytes += (uint32_t)p.bs * (kDim + 4);
+          }
+        }
+        desc[s].b = b;
+        desc[s].tile = (int)i;
+        desc[s].missing = missing;
+        bar_expect(full, bytes);
+        for (int c = 0; c < nblk; ++c) {
+          if (missing >> c & 1u) continue;
+          tma_3d(st + kOff + (uint32_t)(c * p.bs * kDim), &kmap, 0, 0, blk_id[c], full);
+          bulk_copy(st + scOff + (uint32_t)(c * p.bs * 4),
+                    p.kv + (int64_t)blk_id[c] * p.bs * (kDim + 4) + (int64_t)p.bs * kDim,
+                    (uint32_t)p.bs * 4, full);
+        }
+        tma_2d(st + qOff, &qmap, 0, p.qrow0 + b * N, full);
+        bulk_copy(st + wOff, p.w + (int64_t)b * N, (uint32_t)N * 4, full);
+        ++w;
+        ++i;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
+      for (;; ++issued) {
+        const int s = (int)(issued % S);
+        const int a = (int)(issued & 1);
+        if (!wait_phase(bar_full + 8 * s, (uint32_t)((issued / S) & 1))) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeoutBit);
+          break;
+        }
+        if (issued >= 2 && !wait_phase(bar_acce + 8 * a, (uint32_t)(((issued >> 1) - 1) & 1))) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeoutBit);
+          break;
+        }
+        if (desc[s].b < 0) {          // end of range: pass the marker to the epilogue
+          bar_arrive(bar_accf + 8 * a);
+          ++issued;
+          break;
+        }
+        if (*abort_flag) break;
+        tc_fence_after();
+        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
+        const uint64_t da = smem_desc(st + kOff), db = smem_desc(st + qOff);
+        const uint32_t d = tmem + (uint32_t)(a * N);
+#pragma unroll
+        for (int k = 0; k < kDim / 32; ++k) tc_mma(d, da + 2 * k, db + 2 * k, idesc, k);
+        tc_commit(bar_accf + 8 * a);
+        tc_commit(bar_empty + 8 * s);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;       // token within the tile
+    for (int64_t n = 0;; ++n) {
+      const int s = (int)(n % S);
+      const int a = (int)(n & 1);
+      if (!wait_phase(bar_accf + 8 * a, (uint32_t)((n >> 1) & 1))) {
+        *abort_flag = 1;
+        report(p.err, kErrTimeoutBit);
+        break;
+      }
+      // the stage's full barrier has completed for this tile (its refill
+      // needs this warp's release): waiting on it again makes the
+      // producer's descriptor and the copied scales / weights visible here
+      if (!wait_phase(bar_full + 8 * s, (uint32_t)((n / S) & 1))) {
+        *abort_flag = 1;
+        report(p.err, kErrTimeoutBit);
+        break;
+      }
+      const TileDesc d = desc[s];
+      if (d.b < 0 || *abort_flag) break;
+      tc_fence_after();
+      const unsigned char* st = gbase + (size_t)s * p.stage_bytes;
+      const float scale = reinterpret_cast<const float*>(st + scOff)[row];
+      const float* wts = reinterpret_cast<const float*>(st + wOff);
+      const bool missing = (d.missing >> (row / p.bs)) & 1u;
+      const int64_t t = (int64_t)d.tile * kTile + row;
+      float out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        out[j] = 0.f;
+        if (j < p.next_n) {
+          float acc = 0.f;
+          for (int c = 0; c < p.H; c += 16) {
+            float v[16];
+            tc_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N + j * p.H + c), v);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc = fmaf(wts[j * p.H + c + k], fmaxf(v[k], 0.f), acc);
+          }
+          out[j] = scale * acc;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive(bar_acce + 8 * a);
+        bar_arrive(bar_empty + 8 * s);
+      }
+      const int64_t cb = ctxc[d.b];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < p.next_n && t < row_len(cb, p.next_n, j, p.max_len))
+          p.logits[((int64_t)d.b * p.next_n + j) * p.ld + t] = missing ? -INFINITY : out[j];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let this CTA's copies and MMAs finish before the memory and TMEM go away
+    if (warp == 0 && lane == 0) {
+      const int64_t first = issued > S ? issued - S : 0;
+      for (int64_t m = first; m < issued; ++m)
+        wait_phase(bar_full + 8 * (int)(m % S), (uint32_t)((m / S) & 1));
+    }
+    if (warp == 1 && lane == 0 && issued > 0) {
+      const int64_t m = issued - 1;
+      wait_phase(bar_accf + 8 * (int)(m & 1), (uint32_t)((m >> 1) & 1));
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(p.tmem_cols)
+                 : "memory");
+  }
+}
+
+// -inf for each row's columns [L_r, max_len)
+__global__ void fill_kernel(float* logits, int64_t ld, const int32_t* ctx, int next_n,
+                            int64_t max_len) {
+  const int r = blockIdx.x;
+  const int64_t L = row_len(ctx[r / next_n], next_n, r % next_n, max_len);
+  float* row = logits + (int64_t)r * ld;
+  for (int64_t t = L + threadIdx.x; t < max_len; t += blockDim.x) row[t] = -INFINITY;
+}
+
+// --- top-k per row -----------------------------------------------------------
+
+constexpr int kTkThreads = 1024;
+constexpr int kTkMax = QSA_IDX_MAX_TOPK;   // 2048
+
+struct TkParams {
+  const float* logits;
+  int64_t s0, s1, num_cols;
+  const int32_t* seq_lens;
+  int next_n;
+  int topk;
+  int32_t* out;
+  int64_t out_s0;
+};
+
+struct TkShared {
+  unsigned long long sel[kTkMax];
+  uint32_t hist[2048];
+  uint32_t wsum[32];
+  uint32_t digit, above, total;
+  int cnt_above;
+};
+
+// Unsigned key with the order of the float (-0 taken as +0: they are equal).
+__device__ __forceinline__ uint32_t ordered(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// hist[0..nb): the digit d with above(d) < need <= above(d) + hist[d], where
+// above(d) counts the keys in digits above d.
+__device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nb / kTkThreads;
+  uint32_t local = 0;
+  for (int k = 0; k < per; ++k) local += sh.hist[tid * per + k];
+  uint32_t suf = local;                       // inclusive suffix within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  if (lane == 0) sh.wsum[warp] = suf;
+  __syncthreads();
+  uint32_t above = suf - local;               // keys in this warp's higher threads
+  for (int w2 = warp + 1; w2 < 32; ++w2) above += sh.wsum[w2];
+  for (int k = per - 1; k >= 0; --k) {
+    const uint32_t h = sh.hist[tid * per + k];
+    if (above < need && need <= above + h) {
+      sh.digit = (uint32_t)(tid * per + k);
+      sh.above = above;
+    }
+    above += h;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTkThreads, 1) topk_rows_kernel(const TkParams p) {
+  extern __shared__ unsigned char tk_raw[];
+  TkShared& sh = *reinterpret_cast<TkShared*>(tk_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = blockIdx.x;
+  int64_t L = (int64_t)p.seq_lens[r / p.next_n] - p.next_n + (r % p.next_n) + 1;
+  L = L < p.num_cols ? L : p.num_cols;
+  L = L > 0 ? L : 0;
+  const int K = (int)(L < p.topk ? L : p.topk);
+  int32_t* out = p.out + (int64_t)r * p.out_s0;
+  const float* row = p.logits + (int64_t)r * p.s0;
+  if (K == 0) {
+    for (int i = tid; i < p.topk; i += kTkThreads) out[i] = -1;
+    return;
+  }
+  const auto pair = [](uint32_t key, int64_t t) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+  };
+  if (L <= p.topk) {
+    for (int64_t t = tid; t < L; t += kTkThreads) sh.sel[t] = pair(ordered(row[t * p.s1]), t);
+  } else {
+    uint32_t prefix = 0, mask = 0, need = (uint32_t)K;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int ps = 0; ps < 3; ++ps) {
+      const int nb = 1 << widths[ps];
+      for (int i = tid; i < 2048; i += kTkThreads) sh.hist[i] = 0;
+      __syncthreads();
+      for (int64_t t = tid; t < L; t += kTkThreads) {
+        const uint32_t k = ordered(row[t * p.s1]);
+        if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shifts[ps]) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      tk_find_digit(sh, nb < kTkThreads ? kTkThreads : nb, need);
+      prefix |= sh.digit << shifts[ps];
+      mask |= (uint32_t)(nb - 1) << shifts[ps];
+      need -= sh.above;
+      __syncthreads();
+    }
+    const uint32_t T = prefix;                 // the K-th largest key; `need` ties kept
+    if (tid == 0) sh.cnt_above = 0;
+    __syncthreads();
+    uint32_t running = 0;
+    for (int64_t b0 = 0; b0 < L; b0 += kTkThreads) {
+      const int64_t t = b0 + tid;
+      const uint32_t k = t < L ? ordered(row[t * p.s1]) : 0u;
+      if (t < L && k > T) sh.sel[atomicAdd(&sh.cnt_above, 1)] = pair(k, t);
+      const bool tie = t < L && k == T;
+      const uint32_t bal = __ballot_sync(0xffffffffu, tie);
+      if (lane == 0) sh.wsum[warp] = __popc(bal);
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t v = sh.wsum[lane];
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        sh.wsum[lane] = incl - v;
+        if (lane == 31) sh.total = incl;
+      }
+      __syncthreads();
+      const uint32_t rank = running + sh.wsum[warp] + __popc(bal & ((1u << lane) - 1u));
+      if (tie && rank < need) sh.sel[(uint32_t)K - need + rank] = pair(k, t);
+      running += sh.total;
+      __syncthreads();
+    }
+  }
+  for (int i = K + tid; i < kTkMax; i += kTkThreads) sh.sel[i] = 0ull;
+  __syncthreads();
+  // bitonic sort, descending
+  for (int kk = 2; kk <= kTkMax; kk <<= 1) {
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      const int lo = ((tid & ~(jj - 1)) << 1) | (tid & (jj - 1));
+      const int hi = lo + jj;
+      const unsigned long long x = sh.sel[lo], y = sh.sel[hi];
+      const bool desc_order = (lo & kk) == 0;
+      if (desc_order ? (x < y) : (x > y)) {
+        sh.sel[lo] = y;
+        sh.sel[hi] = x;
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < p.topk; i += kTkThreads)
+    out[i] = i < K ? (int32_t)(0xFFFFFFFFu - (uint32_t)(sh.sel[i] & 0xFFFFFFFFull)) : -1;
+}
+
+// --- host side -----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool ready = false;
+};
+
+cudaError_t dev_info(DevInfo** out) {
+  static std::mutex mu;
+  static DevInfo info[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  DevInfo& d = info[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kLogitSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(TkShared));
+    if (e != cudaSuccess) return e;
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+struct Span {
+  uintptr_t lo, hi;
+};
+Span span(const void* p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Span{lo, lo + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+}  // namespace
+}  // namespace qsa
+
+extern "C" qsa_status qsa_paged_mqa_logits(
+    const void* q, qsa_dtype q_dtype, int64_t num_rows, int64_t num_heads, const void* kv_cache,
+    qsa_dtype kv_dtype, int64_t num_blocks, int64_t block_size, const void* weights,
+    qsa_dtype weights_dtype, const void* context_lens, qsa_dtype ctx_dtype, int64_t batch,
+    const void* block_tables, qsa_dtype bt_dtype, int64_t bt_cols, int64_t bt_stride0,
+    int64_t next_n, void* logits, qsa_dtype logits_dtype, int64_t max_model_len,
+    int64_t logits_stride0, uint32_t* error_word, qsa_stream_t stream) {
+  using namespace qsa;
+  if (q_dtype != QSA_DT_F8E4M3 || kv_dtype != QSA_DT_F8E4M3) return QSA_ERR_DTYPE;
+  if (weights_dtype != QSA_DT_F32 || logits_dtype != QSA_DT_F32) return QSA_ERR_DTYPE;
+  if (ctx_dtype != QSA_DT_I32 || bt_dtype != QSA_DT_I32) return QSA_ERR_DTYPE;
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
+    return QSA_ERR_SHAPE;
+  if (next_n < 1 || next_n > 4 || num_heads * next_n > kMaxN) return QSA_ERR_SHAPE;
+  if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 &&
+      block_size != 128)
+    return QSA_ERR_SHAPE;
+  if (batch < 0 || num_rows != batch * next_n || num_rows > INT32_MAX / 256) return QSA_ERR_SHAPE;
+  if (num_blocks < 0 || num_blocks > INT32_MAX || bt_cols < 0 || bt_cols > INT32_MAX ||
+      max_model_len < 0 || max_model_len > INT32_MAX)
+    return QSA_ERR_SHAPE;
+  if (bt_stride0 < bt_cols || logits_stride0 < max_model_len) return QSA_ERR_STRIDE;
+  if (num_rows == 0 || max_model_len == 0) return QSA_OK;
+  if (!q || !weights || !context_lens || !logits) return QSA_ERR_NULL;
+  if (num_blocks > 0 && !kv_cache) return QSA_ERR_NULL;
+  if (bt_cols > 0 && !block_tables) return QSA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) ||
+      !aligned(context_lens, 4) || !aligned(block_tables, 4) || !aligned(logits, 4) ||
+      !aligned(error_word, 4))
+    return QSA_ERR_ALIGN;
+  const int64_t H = num_heads, N = H * next_n;
+  const Span out = span(logits, ((num_rows - 1) * logits_stride0 + max_model_len) * 4);
+  const Span ins[5] = {span(q, num_rows * H * kDim),
+                       span(kv_cache, num_blocks * block_size * (kDim + 4)),
+                       span(weights, num_rows * H * 4), span(context_lens, batch * 4),
+                       span(block_tables, bt_cols > 0 ? ((batch - 1) * bt_stride0 + bt_cols) * 4 : 0)};
+  for (const Span& s : ins)
+    if (overlaps(out, s)) return QSA_ERR_ALIAS;
+  if (error_word && (overlaps(span(error_word, 4), out))) return QSA_ERR_ALIAS;
+
+  DevInfo* di = nullptr;
+  if (dev_info(&di) != cudaSuccess) return QSA_ERR_CUDA;
+  auto fn = encode_fn();
+  if (!fn) return QSA_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  CUtensorMap kmap, qmap;
+  memset(&kmap, 0, sizeof(kmap));
+  memset(&qmap, 0, sizeof(qmap));
+  if (num_blocks > 0) {
+    cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)kDim, (cuuint64_t)(block_size * (kDim + 4))};
+    cuuint32_t box[3] = {(cuuint32_t)kDim, (cuuint32_t)block_size, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (fn(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv_cache), dims, strides,
+           box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QSA_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)(num_rows * H)};
+    cuuint64_t strides[1] = {(cuuint64_t)kDim};
+    cuuint32_t box[2] = {(cuuint32_t)kDim, (cuuint32_t)N};
+    cuuint32_t es[2] = {1, 1};
+    if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(q), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QSA_ERR_CUDA;
+  }
+  const int32_t* ctx = static_cast<const int32_t*>(context_lens);
+  float* lg = static_cast<float*>(logits);
+  fill_kernel<<<(unsigned)num_rows, 256, 0, st>>>(lg, logits_stride0, ctx, (int)next_n,
+                                                  max_model_len);
+  const int stage_raw = (int)(kTile * kDim + N * kDim + kTile * 4 + N * 4);
+  const int stage_bytes = (stage_raw + 1023) & ~1023;
+  const int stages =
+      (int)std::min<int64_t>(kMaxStages, (int64_t)(kLogitSmem - 1024 - kMiscBytes - kTablesBytes) /
+                                             stage_bytes);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * N)) cols <<= 1;
+  const int64_t tiles_per_req = (max_model_len + kTile - 1) / kTile;
+  for (int64_t b0 = 0; b0 < batch; b0 += kMaxBatch) {
+    const int nb = (int)std::min<int64_t>(kMaxBatch, batch - b0);
+    LogitParams p{};
+    p.kv = static_cast<const uint8_t*>(kv_cache);
+    p.w = static_cast<const float*>(weights) + b0 * N;
+    p.ctx = ctx + b0;
+    p.bt = static_cast<const int32_t*>(block_tables) + (bt_cols > 0 ? b0 * bt_stride0 : 0);
+    p.num_blocks = num_blocks;
+    p.bt_cols = bt_cols;
+    p.bt_s0 = bt_stride0;
+    p.logits = lg + b0 * next_n * logits_stride0;
+    p.ld = logits_stride0;
+    p.max_len = max_model_len;
+    p.err = error_word;
+    p.bs = (int)block_size;
+    p.H = (int)H;
+    p.next_n = (int)next_n;
+    p.N = (int)N;
+    p.batch = nb;
+    p.qrow0 = (int)(b0 * N);
+    p.stage_bytes = stage_bytes;
+    p.stages = stages;
+    p.tmem_cols = cols;
+    const int64_t items = (int64_t)nb * tiles_per_req;
+    const int grid = (int)std::min<int64_t>(items, di->sms);
+    logits_kernel<<<grid, kLogitThreads, kLogitSmem, st>>>(p, kmap, qmap);
+  }
+  return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+extern "C" qsa_status qsa_top_k_per_row_decode(
+    const void* logits, qsa_dtype logits_dtype, int64_t num_rows, int64_t num_cols,
+    int64_t stride0, int64_t stride1, int64_t next_n, const void* seq_lens,
+    qsa_dtype seq_lens_dtype, int64_t batch, int64_t topk_tokens, void* indices,
+    qsa_dtype idx_dtype, int64_t idx_stride0, qsa_stream_t stream) {
+  using namespace qsa;
+  if (logits_dtype != QSA_DT_F32 || seq_lens_dtype != QSA_DT_I32 || idx_dtype != QSA_DT_I32)
+    return QSA_ERR_DTYPE;
+  if (next_n < 1 || batch < 0 || num_rows != batch * next_n || num_rows > INT32_MAX)
+    return QSA_ERR_SHAPE;
+  if (num_cols < 0 || num_cols > INT32_MAX) return QSA_ERR_SHAPE;
+  if (topk_tokens < 1 || topk_tokens > kTkMax) return QSA_ERR_CONTRACT;
+  if (stride1 < 1 || stride0 < 0 || idx_stride0 < topk_tokens) return QSA_ERR_STRIDE;
+  if (num_rows > 1 && stride0 < 1) return QSA_ERR_STRIDE;
+  if (num_rows == 0) return QSA_OK;
+  if (!seq_lens || !indices || (num_cols > 0 && !logits)) return QSA_ERR_NULL;
+  if (!aligned(logits, 4) || !aligned(seq_lens, 4) || !aligned(indices, 4)) return QSA_ERR_ALIGN;
+  const Span out = span(indices, ((num_rows - 1) * idx_stride0 + topk_tokens) * 4);
+  const int64_t lg_extent =
+      num_cols > 0 ? ((num_rows - 1) * stride0 + (num_cols - 1) * stride1 + 1) * 4 : 0;
+  if (overlaps(out, span(logits, lg_extent)) || overlaps(out, span(seq_lens, batch * 4)))
+    return QSA_ERR_ALIAS;
+  DevInfo* di = nullptr;
+  if (dev_info(&di) != cudaSuccess) return QSA_ERR_CUDA;
+  TkParams p{};
+  p.logits = static_cast<const float*>(logits);
+  p.s0 = stride0;
+  p.s1 = stride1;
+  p.num_cols = num_cols;
+  p.seq_lens = static_cast<const int32_t*>(seq_lens);
+  p.next_n = (int)next_n;
+  p.topk = (int)topk_tokens;
+  p.out = static_cast<int32_t*>(indices);
+  p.out_s0 = idx_stride0;
+  topk_rows_kernel<<<(unsigned)num_rows, kTkThreads, sizeof(TkShared), (cudaStream_t)stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}

@@ -297,3 +297,80 @@ def _permuted_single(name, L, cmp_pool, kv_pool, seed, device, cmp_dtype="fp16")
         q_attn=q_attn, kv_cache=kv, kv_page_table=kv_pt.to(device),
         meta={"seed": seed, "cmp_pool": cmp_pool, "kv_pool": kv_pool})
 
+
+
+# --- weighted paged MQA indexer (DeepSeek-V3.2 style) -----------------------
+
+IDX_DIM = 128
+
+
+@dataclass
+class IndexerBatch:
+    """Inputs of the indexer decode step: rows r = b*next_n + j.
+
+    q             float8_e4m3fn [rows, heads, 128]
+    kv_cache      uint8 [num_blocks, block_size*132]: per block the tokens'
+                  128 E4M3 value bytes, then their fp32 scales
+    weights       float32 [rows, heads]
+    context_lens  int32 [batch]
+    block_tables  int32 [batch, cols] (-1 = unused column)
+    """
+    name: str
+    q: torch.Tensor
+    kv_cache: torch.Tensor
+    weights: torch.Tensor
+    context_lens: torch.Tensor
+    block_tables: torch.Tensor
+    next_n: int
+    block_size: int
+    max_model_len: int
+    meta: dict = field(default_factory=dict)
+
+
+def indexer_batch(name: str, context_lens: list[int], *, next_n: int = 1, heads: int = 64,
+                  block_size: int = 64, max_model_len: int | None = None,
+                  extra_blocks: int = 3, tie_values: int = 0, seed: int = 0,
+                  device="cpu") -> IndexerBatch:
+    """Seeded indexer inputs.  Query values ~ N(0, 2^2), key values
+    ~ N(0, 16^2), both rounded to E4M3; key scales ~ U[0.005, 0.05]; head
+    weights ~ N(0, 1/8^2).  Each request's blocks are drawn without
+    replacement from one random permutation of the pool (``extra_blocks``
+    spare blocks).  ``tie_values`` > 0 draws every key from that many random
+    vectors with one common scale (exact logit ties)."""
+    B = len(context_lens)
+    rows = B * next_n
+    sg = torch.Generator().manual_seed(seed)
+    need = [(max(c, 0) + block_size - 1) // block_size for c in context_lens]
+    nblocks = max(1, sum(need) + extra_blocks)
+    cols = max(1, max(need))
+    perm = torch.randperm(nblocks, generator=sg)
+    bt = torch.full((B, cols), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(need):
+        if n:
+            bt[b, :n] = perm[at:at + n].to(torch.int32)
+        at += n
+    vg = torch.Generator(device=device).manual_seed(seed + 1)
+    q = (torch.randn((rows, heads, IDX_DIM), generator=vg, device=device) * 2.0).to(
+        torch.float8_e4m3fn)
+    w = torch.randn((rows, heads), generator=vg, device=device) / 8.0
+    ntok = nblocks * block_size
+    if tie_values:
+        vecs = (torch.randn((tie_values, IDX_DIM), generator=vg, device=device) * 16.0).to(
+            torch.float8_e4m3fn)
+        pick = torch.randint(0, tie_values, (ntok,), generator=sg).to(device)
+        vals = vecs.view(torch.uint8)[pick]
+        scales = torch.full((ntok,), 0.02, dtype=torch.float32, device=device)
+    else:
+        vals = (torch.randn((ntok, IDX_DIM), generator=vg, device=device) * 16.0).to(
+            torch.float8_e4m3fn).view(torch.uint8)
+        scales = torch.rand((ntok,), generator=vg, device=device) * 0.045 + 0.005
+    cache = torch.empty((nblocks, block_size * (IDX_DIM + 4)), dtype=torch.uint8, device=device)
+    cache[:, :block_size * IDX_DIM] = vals.view(nblocks, block_size * IDX_DIM)
+    cache[:, block_size * IDX_DIM:] = scales.view(nblocks, block_size).contiguous().view(
+        torch.uint8).view(nblocks, block_size * 4)
+    mml = max_model_len or max(1, max(context_lens))
+    return IndexerBatch(name=name, q=q, kv_cache=cache, weights=w,
+                        context_lens=torch.tensor(context_lens, dtype=torch.int32).to(device),
+                        block_tables=bt.to(device), next_n=next_n, block_size=block_size,
+                        max_model_len=mml, meta={"seed": seed, "blocks": nblocks})

@@ -220,3 +220,60 @@ def test_metadata_nothing_to_do_and_optional_inputs(lib):
     assert _meta(lib, T=0, maxw=0, work=None, cols=0, bt=None) == 0
     assert _meta(lib, T=0, maxw=0, work=None, t2r=None, lpos=None, vis=None, slot=None,
                  common=None) == 0
+
+
+# --- fail-closed indexer ------------------------------------------------------
+
+def _logits(lib, **over):
+    a = dict(q=_addr(1), qdt=6, rows=8, heads=64, kv=_addr(2), kvdt=6, nblocks=100, bs=64,
+             w=_addr(3), wdt=3, ctx=_addr(4), ctxdt=4, batch=4, bt=_addr(5), btdt=4, cols=16,
+             bts0=16, next_n=2, out=_addr(10), odt=3, mml=4096, ld=4096, err=None, stream=None)
+    a.update(over)
+    return lib.qsa_paged_mqa_logits(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qdt=1), 2), (dict(kvdt=1), 2), (dict(wdt=1), 2), (dict(odt=1), 2), (dict(ctxdt=5), 2),
+    (dict(btdt=5), 2),
+    (dict(heads=48), 3), (dict(heads=8), 3), (dict(next_n=0), 3), (dict(next_n=5), 3),
+    (dict(heads=128, next_n=4, rows=16), 3), (dict(bs=48), 3), (dict(bs=4), 3),
+    (dict(rows=9), 3), (dict(batch=-1), 3), (dict(nblocks=-1), 3), (dict(mml=-1), 3),
+    (dict(bts0=8), 4), (dict(ld=100), 4),
+    (dict(q=None), 1), (dict(w=None), 1), (dict(ctx=None), 1), (dict(out=None), 1),
+    (dict(kv=None), 1), (dict(bt=None), 1),
+    (dict(q=_addr(1) + 8), 5), (dict(kv=_addr(2) + 4), 5), (dict(w=_addr(3) + 4), 5),
+    (dict(ctx=_addr(4) + 2), 5), (dict(out=_addr(10) + 2), 5),
+    (dict(out=_addr(1)), 8), (dict(out=_addr(2) + 4096), 8), (dict(out=_addr(5)), 8),
+    (dict(err=_addr(10) + 64), 8),
+])
+def test_paged_mqa_logits_fails_closed(lib, over, status):
+    assert _logits(lib, **over) == status
+
+
+def test_paged_mqa_logits_nothing_to_do(lib):
+    assert _logits(lib, rows=0, batch=0) == 0
+    assert _logits(lib, mml=0, ld=0) == 0
+
+
+def _topk(lib, **over):
+    a = dict(lg=_addr(1), lgdt=3, rows=8, cols=4096, s0=4096, s1=1, next_n=2, sl=_addr(2),
+             sldt=4, batch=4, topk=2048, out=_addr(10), odt=4, os0=2048, stream=None)
+    a.update(over)
+    return lib.qsa_top_k_per_row_decode(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(lgdt=1), 2), (dict(sldt=5), 2), (dict(odt=5), 2),
+    (dict(rows=9), 3), (dict(next_n=0), 3), (dict(cols=-1), 3),
+    (dict(topk=0), 6), (dict(topk=2049), 6),
+    (dict(s1=0), 4), (dict(os0=100), 4), (dict(s0=0), 4),
+    (dict(lg=None), 1), (dict(sl=None), 1), (dict(out=None), 1),
+    (dict(lg=_addr(1) + 2), 5), (dict(out=_addr(10) + 2), 5),
+    (dict(out=_addr(1)), 8), (dict(out=_addr(2)), 8),
+])
+def test_top_k_per_row_fails_closed(lib, over, status):
+    assert _topk(lib, **over) == status
+
+
+def test_top_k_per_row_nothing_to_do(lib):
+    assert _topk(lib, rows=0, batch=0) == 0
