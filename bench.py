@@ -586,6 +586,25 @@ def spec_variant(args, R, world, rank, dev, stream, peak):
             "frac_of_peak_keys_shared": (uniq_sel + att) / (ms * 1e-3) / 1e9 / peak}
 
 
+def run_indexer_only(args, world, rank, local):
+    """Only the indexer measurement, printed as its own JSON object (a small,
+    self-contained case for profiling its kernels)."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    from sparse_paged_attention_qsa_gb300 import build as qbuild
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the product path has no CPU fallback)")
+    qbuild.build()
+    qsa.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    peak, _ = _peaks()
+    res = indexer_variant(args, world, rank, dev, torch.cuda.current_stream(dev), peak)
+    if rank == 0:
+        print(json.dumps({"paged_mqa_indexer": res}), flush=True)
+    return 0
+
+
 def indexer_variant(args, world, rank, dev, stream, peak):
     """The weighted paged MQA indexer decode step (DeepSeek-V3.2 style):
     128 requests x 2 query tokens x 64 heads over 65536 cached tokens each
@@ -662,12 +681,16 @@ def main():
                     help="skip the speculative-decode (4 tokens per request) measurement")
     ap.add_argument("--no-indexer", action="store_true",
                     help="skip the paged MQA indexer measurement")
+    ap.add_argument("--indexer-only", action="store_true",
+                    help="run only the paged MQA indexer measurement (profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps are required")
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.indexer_only:
+        return run_indexer_only(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

@@ -8,19 +8,23 @@
 // (see the header): logit = key scale * sum_h w_h * ReLU(q_h . k).
 //
 // logits_kernel  persistent, one CTA per SM, warp-specialised:
-//   warp 0  producer: per 128-token tile of one request, TMA loads of the
-//           tile's cache blocks (128-byte value rows, 128-byte swizzle), the
-//           request's query rows (all heads of its next_n tokens, same
-//           swizzle), and plain bulk copies of the blocks' scales and the
-//           rows' head weights, into a ring of shared-memory stages;
+//   warp 0  producer: per 128-token tile of one request, each lane loads one
+//           of the tile's cache blocks -- a TMA of its 128-byte value rows
+//           (128-byte swizzle) and a bulk copy of its scales -- into a ring
+//           of shared-memory stages, the block ids fetched a tile ahead;
+//           the request's query rows (all heads of its next_n tokens, same
+//           swizzle) and head weights go to one of two query slots once per
+//           request the CTA works on;
 //   warp 1  one lane issues four tcgen05.mma kind::f8f6f4 (M = 128 tokens,
-//           N = next_n x heads, K = 32 each) per tile into one of two TMEM
-//           accumulators, then commits to the accumulator's and the stage's
+//           N = next_n x heads, K = 32 each) per tile into one of four TMEM
+//           accumulators (two when N = 256), then commits to the accumulator's and the stage's
 //           barriers; the warp owns the TMEM allocation;
-//   warps 2-5  epilogue: each thread owns one token (its TMEM lane), reads
-//           its accumulator row 16 columns at a time (tcgen05.ld), forms
-//           sum_h w_h * ReLU(d_h) per query row in fp32, scales, and writes
-//           the logits (consecutive threads, consecutive columns).
+//   warps 2-9  epilogue in two groups of four warps (one warp per TMEM lane
+//           quarter) taking alternate tiles: each thread owns one token (its
+//           TMEM lane), reads its accumulator row with one tcgen05.ld per 64
+//           columns, forms sum_h w_h * ReLU(d_h) for every query row in fp32
+//           (packed pairs), scales, and writes the logits (consecutive
+//           threads, consecutive columns).
 // fill_kernel    writes -inf to each row's columns [L_r, max_model_len).
 // topk_rows_kernel  one CTA per row: exact radix select (11/11/10 bits) of
 //           the k-th largest ordered logit, emission of the larger ones and
@@ -48,9 +52,20 @@ namespace {
 constexpr int kDim = QSA_IDX_HEAD_DIM;      // 128 E4M3 values per query head / key
 constexpr int kTile = 128;                  // tokens per tile (MMA M)
 constexpr int kMaxN = 256;                  // next_n x heads (MMA N)
-constexpr int kLogitThreads = 6 * 32;
+#ifndef QSA_IDX_EPI_GROUPS
+#define QSA_IDX_EPI_GROUPS 2
+#endif
+// Epilogue groups taking tiles in turn.  A group always owns the same
+// accumulators (tile n uses accumulator n % NA and group n % G with G
+// dividing NA), so no warp can wait on an accumulator's barrier phase before
+// the previous phase has completed.
+constexpr int kEpiGroups = QSA_IDX_EPI_GROUPS;
+constexpr int kEpiWarps = 4 * kEpiGroups;       // one warp per TMEM lane quarter per group
+constexpr int kLogitThreads = (2 + kEpiWarps) * 32;
 constexpr int kMaxBatch = 1024;             // requests per launch (tables in smem)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kMaxAcc = 4;                  // TMEM accumulators (512 columns / N, at most 4)
+constexpr int kProdTiles = 4;               // tiles the producer arms per iteration
 constexpr size_t kLogitSmem = 220 * 1024;
 constexpr size_t kTablesBytes = (size_t)(kMaxBatch + 1) * 8 + (size_t)kMaxBatch * 4;
 constexpr size_t kMiscBytes = 1024;         // barriers + stage descriptors
@@ -70,15 +85,19 @@ struct LogitParams {
   int bs, H, next_n, N;
   int batch;                  // requests in this launch
   int qrow0;                  // query-map row of this launch's first request (b0 * N)
-  int stage_bytes, stages;
+  int stage_bytes, stages;    // stage: tile values (16 KiB) + scales (512 B)
+  int qslot_bytes;            // query slot: N*128 query bytes + N*4 weights
+  int nacc;                   // TMEM accumulators of N columns
+  int bs_log2;                // log2(bs)
   uint32_t tmem_cols;
 };
 
 struct TileDesc {
-  int b;          // request within the launch; -1: no more work
-  int tile;       // tile index within the request
+  int b;             // request within the launch; -1: no more work
+  int tile;          // tile index within the request
   uint32_t missing;  // bit c: block c of the tile had no valid cache block
-  int pad;
+  uint32_t qinfo;    // bit 0: query slot, bit 1: its phase, bit 2: the
+                     // request's last tile in this CTA (frees the slot)
 };
 
 // --- PTX helpers -------------------------------------------------------------
@@ -88,16 +107,28 @@ __device__ __forceinline__ uint64_t gtime() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ bool try_wait(uint32_t a, uint32_t ph) {
+// Test the phase; a thread whose phase is not complete is suspended until it
+// completes or about 20 us pass (the hint), so waiting warps do not take
+// issue slots from the warps doing the work.
+__device__ __forceinline__ bool try_wait(uint32_t a, uint32_t ph, uint32_t hint_ns = 20000u) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(a), "r"(ph), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+// Non-blocking test of a phase (cheaper than try_wait when it has completed).
+__device__ __forceinline__ bool test_wait(uint32_t a, uint32_t ph) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(a), "r"(ph) : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ bool wait_phase(uint32_t a, uint32_t ph) {
-  if (try_wait(a, ph)) return true;
+  if (test_wait(a, ph)) return true;
   const uint64_t t0 = gtime();
   while (!try_wait(a, ph))
     if (gtime() - t0 > kWaitNs) return false;
@@ -160,18 +191,67 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// NC accumulator columns of this thread's TMEM lane in one load; the wait is
+// in the same asm statement, so no use of the outputs can precede it.
+template <int NC>
+__device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&r)[NC]);
+template <>
+__device__ __forceinline__ void tc_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-      " [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tc_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tc_ld<64>(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// sum over the NC columns from c0 of w[c] * ReLU(d[c]) for this thread's TMEM
+// lane (taddr addresses column 0 of its accumulator): one TMEM load, then
+// four fp32 chains (packed in pairs)
+template <int NC>
+__device__ __forceinline__ float head_sum_n(uint32_t taddr, const float* w, int c0) {
+  uint32_t r[NC];
+  tc_ld<NC>(taddr + (uint32_t)c0, r);
+  const float4* w4 = reinterpret_cast<const float4*>(w + c0);
+  float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int k = 0; k < NC; k += 4) {
+    const float4 ww = w4[k / 4];
+    lo = ffma2(make_float2(ww.x, ww.y),
+               make_float2(fmaxf(__uint_as_float(r[k + 0]), 0.f),
+                           fmaxf(__uint_as_float(r[k + 1]), 0.f)), lo);
+    hi = ffma2(make_float2(ww.z, ww.w),
+               make_float2(fmaxf(__uint_as_float(r[k + 2]), 0.f),
+                           fmaxf(__uint_as_float(r[k + 3]), 0.f)), hi);
+  }
+  return (lo.x + lo.y) + (hi.x + hi.y);
+}
+
+// columns [c0, c0 + nc), nc in {16, 32, 64}
+__device__ __forceinline__ float head_sum(uint32_t taddr, const float* w, int c0, int nc) {
+  switch (nc) {
+    case 16: return head_sum_n<16>(taddr, w, c0);
+    case 32: return head_sum_n<32>(taddr, w, c0);
+    default: return head_sum_n<64>(taddr, w, c0);
+  }
 }
 
 __device__ __forceinline__ int64_t row_len(int64_t ctx, int next_n, int j, int64_t max_len) {
@@ -182,12 +262,15 @@ __device__ __forceinline__ int64_t row_len(int64_t ctx, int next_n, int j, int64
 
 // --- logits ------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kLogitThreads, 1)
+// up to 5 warps share an SM sub-partition's 16K registers: cap the registers
+// so they fit
+__global__ void __maxnreg__(kEpiGroups > 3 ? 96 : (kEpiGroups > 2 ? 128 : 168))
 logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int64_t s_end_tile;                          // first tile index past the range
   __shared__ int64_t s_part[kLogitThreads];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -195,26 +278,37 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
   const uint32_t base = raw + pad;
   unsigned char* gbase = smem_raw + pad;
   const int S = p.stages;
-  const uint32_t misc = base + (uint32_t)(S * p.stage_bytes);
-  const uint32_t bar_full = misc, bar_empty = misc + 8 * kMaxStages;
-  const uint32_t bar_accf = misc + 16 * kMaxStages, bar_acce = bar_accf + 16;
-  TileDesc* desc = reinterpret_cast<TileDesc*>(gbase + S * p.stage_bytes + 16 * kMaxStages + 32);
-  int64_t* pre = reinterpret_cast<int64_t*>(gbase + S * p.stage_bytes + kMiscBytes);
-  int32_t* ctxc = reinterpret_cast<int32_t*>(pre + kMaxBatch + 1);
   const int N = p.N;
-  const uint32_t kOff = 0, qOff = kTile * kDim, scOff = qOff + (uint32_t)N * kDim,
-                 wOff = scOff + kTile * 4;
+  // layout: S stages [values 16 KiB | scales 512 B], two query slots
+  // [query rows N*128 | weights N*4], barriers + descriptors, tables
+  const uint32_t qslots = (uint32_t)(S * p.stage_bytes);
+  const uint32_t misc_off = qslots + 2u * (uint32_t)p.qslot_bytes;
+  const uint32_t misc = base + misc_off;
+  const uint32_t bar_full = misc, bar_empty = misc + 8 * kMaxStages;
+  const uint32_t bar_accf = misc + 16 * kMaxStages, bar_acce = bar_accf + 8 * kMaxAcc;
+  const uint32_t bar_qfull = bar_acce + 8 * kMaxAcc, bar_qempty = bar_qfull + 16;
+  const int NA = p.nacc;                                  // TMEM accumulators
+  TileDesc* desc = reinterpret_cast<TileDesc*>(gbase + misc_off + 16 * kMaxStages + 16 * kMaxAcc + 32);
+  int64_t* pre = reinterpret_cast<int64_t*>(gbase + misc_off + kMiscBytes);
+  int32_t* ctxc = reinterpret_cast<int32_t*>(pre + kMaxBatch + 1);
+  const uint32_t scOff = kTile * kDim;                    // scales within a stage
+  const uint32_t wOff = (uint32_t)N * kDim;               // weights within a query slot
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       bar_init(bar_full + 8 * s, 1);
-      bar_init(bar_empty + 8 * s, 1 + 4);    // MMA commit + 4 epilogue warps
+      bar_init(bar_empty + 8 * s, 1);    // the MMA thread, once the tile's epilogue is done
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kMaxAcc; ++a) {
       bar_init(bar_accf + 8 * a, 1);
-      bar_init(bar_acce + 8 * a, 4);
+      bar_init(bar_acce + 8 * a, 4);     // the four warps of the group that had the tile
+    }
+    for (int k = 0; k < 2; ++k) {
+      bar_init(bar_qfull + 8 * k, 1);
+      bar_init(bar_qempty + 8 * k, 1 + 4);
     }
     s_abort = 0;
+    s_end_tile = INT64_MAX;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -262,150 +356,266 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
   const int64_t w_begin = W * blockIdx.x / gridDim.x;
   const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
   volatile int* abort_flag = &s_abort;
+  volatile int64_t* end_tile = &s_end_tile;
   int64_t issued = 0;    // producer: stages armed; MMA: tiles issued
+  int segs = 0;          // producer: query slots loaded
 
   if (warp == 0) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      int b = 0;
-      int64_t i = 0;
-      if (w_begin < w_end) {
-        int lo = 0, hi = p.batch - 1;     // last request with pre <= w_begin
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (pre[mid] <= w_begin) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-        i = w_begin - pre[b];
+    // ---------------- producer (whole warp) ----------------
+    const int bpt = kTile / p.bs;                     // blocks per tile
+    const auto tiles_of = [&](int bb) { return (int64_t)(ctxc[bb] + kTile - 1) / kTile; };
+    int b = 0;
+    int64_t i = 0, w = w_begin;
+    if (w_begin < w_end) {
+      int lo = 0, hi = p.batch - 1;                   // last request with pre <= w_begin
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= w_begin) lo = mid; else hi = mid - 1;
       }
-      int64_t w = w_begin;
-      const int blocks_per_tile = kTile / p.bs;
-      for (;; ++issued) {
-        const int s = (int)(issued % S);
-        if (issued >= S && !wait_phase(bar_empty + 8 * s, (uint32_t)(((issued / S) - 1) & 1))) {
-          *abort_flag = 1;
-          report(p.err, kErrTimeoutBit);
+      b = lo;
+      i = w_begin - pre[b];
+      while (i >= tiles_of(b)) {
+        ++b;
+        i = 0;
+      }
+    }
+    // up to kProdTiles tiles of one request per iteration; lane = t*bpt + c
+    // handles block c of tile t: it waits for that tile's stage, and the
+    // lanes issue their TMA and scale copies side by side
+    const int bpt_log2 = 7 - p.bs_log2;
+    const int max_t = min(kProdTiles, 32 >> bpt_log2);
+    const int t_lane = lane >> bpt_log2, c_lane = lane & (bpt - 1);
+    // 32 consecutive block-table entries of one request, one per lane, read
+    // in one coalesced load and handed to the tiles by shuffles
+    int chunk_b = -1;
+    int64_t chunk_col0 = 0;
+    int32_t chunk_id = -1;
+    int cur_b = -1, slot = 0;
+    int s = 0, round = 0;                             // ring position of the next stage
+    for (;;) {
+      const int stop = __shfl_sync(0xffffffffu, *abort_flag, 0);
+      if (stop) break;
+      if (w >= w_end) {                 // range done: an end marker in the next stage
+        bool ok = round == 0 || wait_phase(bar_empty + 8 * s, (uint32_t)((round - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report(p.err, kErrTimeoutBit);
+          }
           break;
         }
-        if (*abort_flag) break;
-        if (w >= w_end) {
+        if (lane == 0) {
           desc[s].b = -1;
           bar_arrive(bar_full + 8 * s);
-          ++issued;
+        }
+        ++issued;
+        break;
+      }
+      if (b != cur_b) {                 // a new request: its query rows into the next slot
+        slot = segs & 1;
+        bool ok = segs < 2 || wait_phase(bar_qempty + 8 * slot, (uint32_t)(((segs >> 1) - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report(p.err, kErrTimeoutBit);
+          }
           break;
         }
-        while (i >= (ctxc[b] + kTile - 1) / kTile) {   // skip requests without tiles
-          ++b;
-          i = 0;
+        if (lane == 0) {
+          const uint32_t qf = bar_qfull + 8 * slot;
+          const uint32_t qs = base + qslots + (uint32_t)(slot * p.qslot_bytes);
+          bar_expect(qf, (uint32_t)N * kDim + (uint32_t)N * 4);
+          tma_2d(qs, &qmap, 0, p.qrow0 + b * N, qf);
+          bulk_copy(qs + wOff, p.w + (int64_t)b * N, (uint32_t)N * 4, qf);
         }
-        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const uint32_t full = bar_full + 8 * s;
-        const int64_t tv64 = ctxc[b] - i * kTile;
-        const int tv = (int)(tv64 < kTile ? tv64 : kTile);      // valid tokens in the tile
-        int nblk = (tv + p.bs - 1) / p.bs;
-        uint32_t missing = 0, bytes = (uint32_t)N * kDim + (uint32_t)N * 4;
-        int32_t blk_id[kTile / 8];
-        for (int c = 0; c < nblk; ++c) {
-          const int64_t col = i * blocks_per_tile + c;
-          const int32_t id = col < p.bt_cols ? __ldg(p.bt + (int64_t)b * p.bt_s0 + col) : -1;
-          blk_id[c] = id;
-          if (id < 0 || id >= p.num_blocks) {
-            missing |= 1u << c;
-            report(p.err, kErrBlockBit);
-          } else {
-            bytes += (uint32_t)p.bs * (kDim + 4);
-          }
+        cur_b = b;
+        ++segs;
+      }
+      const int64_t tiles_b = tiles_of(b);
+      const int64_t left = min(tiles_b - i, w_end - w);
+      const int T = (int)(left < max_t ? left : max_t);
+      const bool active = t_lane < T;
+      int st = s + t_lane, rd = round;
+      if (st >= S) {
+        st -= S;
+        ++rd;
+      }
+      bool ok = !active || rd == 0 || wait_phase(bar_empty + 8 * st, (uint32_t)((rd - 1) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeoutBit);
         }
-        desc[s].b = b;
-        desc[s].tile = (int)i;
-        desc[s].missing = missing;
-        bar_expect(full, bytes);
-        for (int c = 0; c < nblk; ++c) {
-          if (missing >> c & 1u) continue;
-          tma_3d(st + kOff + (uint32_t)(c * p.bs * kDim), &kmap, 0, 0, blk_id[c], full);
-          bulk_copy(st + scOff + (uint32_t)(c * p.bs * 4),
-                    p.kv + (int64_t)blk_id[c] * p.bs * (kDim + 4) + (int64_t)p.bs * kDim,
-                    (uint32_t)p.bs * 4, full);
-        }
-        tma_2d(st + qOff, &qmap, 0, p.qrow0 + b * N, full);
-        bulk_copy(st + wOff, p.w + (int64_t)b * N, (uint32_t)N * 4, full);
-        ++w;
-        ++i;
+        break;
+      }
+      const int64_t col0 = i * bpt;     // block-table columns [col0, col0 + T*bpt)
+      if (b != chunk_b || col0 < chunk_col0 || col0 + T * bpt > chunk_col0 + 32) {
+        chunk_b = b;
+        chunk_col0 = col0;
+        const int64_t col = col0 + lane;
+        chunk_id = col < p.bt_cols ? __ldg(p.bt + (int64_t)b * p.bt_s0 + col) : -1;
+      }
+      const int32_t id = __shfl_sync(0xffffffffu, chunk_id, (int)(col0 - chunk_col0) + lane);
+      const int64_t tv = ctxc[b] - (i + t_lane) * kTile;     // tokens left from tile t_lane
+      const int nblk = active ? (int)(((tv < kTile ? tv : kTile) + p.bs - 1) >> p.bs_log2) : 0;
+      const bool inblk = c_lane < nblk;
+      const bool valid = inblk && id >= 0 && id < p.num_blocks;
+      const bool miss = inblk && !valid;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      const uint32_t mmask = __ballot_sync(0xffffffffu, miss);
+      const uint32_t full = bar_full + 8 * st;
+      if (active && c_lane == 0) {      // the tile's lead lane: descriptor and byte count
+        const uint32_t tmask = bpt == 32 ? 0xffffffffu : (1u << bpt) - 1u;
+        const uint32_t vt = (vmask >> (t_lane * bpt)) & tmask;
+        const uint32_t mt = (mmask >> (t_lane * bpt)) & tmask;
+        const bool last = i + t_lane + 1 >= tiles_b || w + t_lane + 1 >= w_end;
+        desc[st].b = b;
+        desc[st].tile = (int)(i + t_lane);
+        desc[st].missing = mt;
+        desc[st].qinfo = (uint32_t)slot | ((uint32_t)(((segs - 1) >> 1) & 1) << 1) |
+                         ((uint32_t)last << 2);
+        bar_expect(full, (uint32_t)__popc(vt) * (uint32_t)p.bs * (kDim + 4));
+        if (mt) report(p.err, kErrBlockBit);
+      }
+      __syncwarp();
+      if (valid) {
+        const uint32_t sb = base + (uint32_t)(st * p.stage_bytes);
+        tma_3d(sb + (uint32_t)(c_lane * p.bs * kDim), &kmap, 0, 0, id, full);
+        bulk_copy(sb + scOff + (uint32_t)(c_lane * p.bs * 4),
+                  p.kv + (int64_t)id * p.bs * (kDim + 4) + (int64_t)p.bs * kDim,
+                  (uint32_t)p.bs * 4, full);
+      }
+      issued += T;
+      w += T;
+      i += T;
+      s += T;
+      if (s >= S) {
+        s -= S;
+        ++round;
+      }
+      while (w < w_end && i >= tiles_of(b)) {
+        ++b;
+        i = 0;
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
-      for (;; ++issued) {
-        const int s = (int)(issued % S);
-        const int a = (int)(issued & 1);
-        if (!wait_phase(bar_full + 8 * s, (uint32_t)((issued / S) & 1))) {
+      int s = 0, round = 0, a = 0, around = 0;         // ring and accumulator positions
+      uint32_t held = 0;                                // stage of the tile in each accumulator (8 bits each)
+      uint32_t seen_q = 0xffffffffu;                    // query slot and phase last waited for
+      for (;; ++issued, s = s + 1 == S ? 0 : s + 1, round += s == 0,
+              a = a + 1 == NA ? 0 : a + 1, around += a == 0) {
+        // accumulator a free again: the epilogue is done with the tile that
+        // used it, so that tile's stage (values, scales) can be refilled
+        if (around > 0) {
+          if (!wait_phase(bar_acce + 8 * a, (uint32_t)((around - 1) & 1))) {
+            *abort_flag = 1;
+            report(p.err, kErrTimeoutBit);
+            break;
+          }
+          bar_arrive(bar_empty + 8 * ((held >> (8 * a)) & 0xffu));
+        }
+        if (!wait_phase(bar_full + 8 * s, (uint32_t)(round & 1))) {
           *abort_flag = 1;
           report(p.err, kErrTimeoutBit);
           break;
         }
-        if (issued >= 2 && !wait_phase(bar_acce + 8 * a, (uint32_t)(((issued >> 1) - 1) & 1))) {
-          *abort_flag = 1;
-          report(p.err, kErrTimeoutBit);
-          break;
-        }
-        if (desc[s].b < 0) {          // end of range: pass the marker to the epilogue
+        held = (held & ~(0xffu << (8 * a))) | ((uint32_t)s << (8 * a));
+        const TileDesc d = desc[s];
+        if (d.b < 0) {                // end of range: tell both epilogue groups
+          // the other groups see the marker while they wait (see below)
+          *end_tile = issued;
           bar_arrive(bar_accf + 8 * a);
           ++issued;
           break;
         }
         if (*abort_flag) break;
+        const int qs = (int)(d.qinfo & 1u);
+        if ((d.qinfo & 3u) != seen_q) {         // a new query slot: wait for its rows
+          if (!wait_phase(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
+            *abort_flag = 1;
+            report(p.err, kErrTimeoutBit);
+            break;
+          }
+          seen_q = d.qinfo & 3u;
+        }
         tc_fence_after();
         const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const uint64_t da = smem_desc(st + kOff), db = smem_desc(st + qOff);
-        const uint32_t d = tmem + (uint32_t)(a * N);
+        const uint64_t da = smem_desc(st);
+        const uint64_t db = smem_desc(base + qslots + (uint32_t)(qs * p.qslot_bytes));
+        const uint32_t dt = tmem + (uint32_t)(a * N);
 #pragma unroll
-        for (int k = 0; k < kDim / 32; ++k) tc_mma(d, da + 2 * k, db + 2 * k, idesc, k);
+        for (int k = 0; k < kDim / 32; ++k) tc_mma(dt, da + 2 * k, db + 2 * k, idesc, k);
         tc_commit(bar_accf + 8 * a);
-        tc_commit(bar_empty + 8 * s);
+        if (d.qinfo & 4u) tc_commit(bar_qempty + 8 * qs);
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9) ----------------
+    // two groups of four warps (one per TMEM lane quarter) take alternate
+    // tiles, so two tiles' waits, TMEM loads and stores overlap; each warp
+    // forms every query row of its tile for its 32 tokens
     const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int group = (warp - 2) >> 2;         // tiles group, group + G, ...
     const int row = quarter * 32 + lane;       // token within the tile
-    for (int64_t n = 0;; ++n) {
-      const int s = (int)(n % S);
-      const int a = (int)(n & 1);
-      if (!wait_phase(bar_accf + 8 * a, (uint32_t)((n >> 1) & 1))) {
+    const int H = p.H;
+    const int G = kEpiGroups < NA ? kEpiGroups : NA;   // active groups (divides NA)
+    int s = group, round = 0, a = group, around = 0;   // position of tile n
+    uint32_t seen_q = 0xffffffffu;                     // query slot and phase last waited for
+    for (int64_t n = group; group < G; n += G) {
+      // wait for tile n's accumulator, or for the end marker to cover tile n
+      // (only the group holding the end tile is woken through the barrier)
+      int state = 0;
+      const uint64_t t0 = gtime();
+      if (test_wait(bar_accf + 8 * a, (uint32_t)(around & 1))) state = 1;
+      while (state == 0) {
+        if (try_wait(bar_accf + 8 * a, (uint32_t)(around & 1), 1000u)) state = 1;
+        else if (n >= *end_tile || *abort_flag) state = 2;
+        else if (gtime() - t0 > kWaitNs) state = 3;
+      }
+      if (state == 3) {
         *abort_flag = 1;
         report(p.err, kErrTimeoutBit);
         break;
       }
+      if (n >= *end_tile || *abort_flag) break;
       // the stage's full barrier has completed for this tile (its refill
-      // needs this warp's release): waiting on it again makes the
-      // producer's descriptor and the copied scales / weights visible here
-      if (!wait_phase(bar_full + 8 * s, (uint32_t)((n / S) & 1))) {
+      // waits for this tile's epilogue): waiting on it again makes the
+      // producer's descriptor and the copied scales visible here
+      if (!wait_phase(bar_full + 8 * s, (uint32_t)(round & 1))) {
         *abort_flag = 1;
         report(p.err, kErrTimeoutBit);
         break;
       }
       const TileDesc d = desc[s];
-      if (d.b < 0 || *abort_flag) break;
+      const int qs = (int)(d.qinfo & 1u);
+      if ((d.qinfo & 3u) != seen_q) {            // a new query slot: its weights visible
+        if (!wait_phase(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
+          *abort_flag = 1;
+          report(p.err, kErrTimeoutBit);
+          break;
+        }
+        seen_q = d.qinfo & 3u;
+      }
       tc_fence_after();
       const unsigned char* st = gbase + (size_t)s * p.stage_bytes;
       const float scale = reinterpret_cast<const float*>(st + scOff)[row];
-      const float* wts = reinterpret_cast<const float*>(st + wOff);
-      const bool missing = (d.missing >> (row / p.bs)) & 1u;
+      const float* wts =
+          reinterpret_cast<const float*>(gbase + qslots + (size_t)qs * p.qslot_bytes + wOff);
+      const bool missing = (d.missing >> (row >> p.bs_log2)) & 1u;
       const int64_t t = (int64_t)d.tile * kTile + row;
-      float out[4];
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N);
+      float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        out[j] = 0.f;
         if (j < p.next_n) {
           float acc = 0.f;
-          for (int c = 0; c < p.H; c += 16) {
-            float v[16];
-            tc_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N + j * p.H + c), v);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc = fmaf(wts[j * p.H + c + k], fmaxf(v[k], 0.f), acc);
-          }
+          for (int c = 0; c < H; c += 64) acc += head_sum(taddr, wts, j * H + c, H < 64 ? H : 64);
           out[j] = scale * acc;
         }
       }
@@ -413,13 +623,23 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       __syncwarp();
       if (lane == 0) {
         bar_arrive(bar_acce + 8 * a);
-        bar_arrive(bar_empty + 8 * s);
+        if (d.qinfo & 4u) bar_arrive(bar_qempty + 8 * qs);
       }
       const int64_t cb = ctxc[d.b];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (j < p.next_n && t < row_len(cb, p.next_n, j, p.max_len))
           p.logits[((int64_t)d.b * p.next_n + j) * p.ld + t] = missing ? -INFINITY : out[j];
+      }
+      s += G;
+      if (s >= S) {
+        s -= S;
+        ++round;
+      }
+      a += G;
+      if (a >= NA) {
+        a -= NA;
+        ++around;
       }
     }
   }
@@ -432,10 +652,12 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       const int64_t first = issued > S ? issued - S : 0;
       for (int64_t m = first; m < issued; ++m)
         wait_phase(bar_full + 8 * (int)(m % S), (uint32_t)((m / S) & 1));
+      for (int g = segs > 2 ? segs - 2 : 0; g < segs; ++g)
+        wait_phase(bar_qfull + 8 * (g & 1), (uint32_t)((g >> 1) & 1));
     }
     if (warp == 1 && lane == 0 && issued > 0) {
       const int64_t m = issued - 1;
-      wait_phase(bar_accf + 8 * (int)(m & 1), (uint32_t)((m >> 1) & 1));
+      wait_phase(bar_accf + 8 * (int)(m % NA), (uint32_t)((m / NA) & 1));
     }
     __syncthreads();
   }
@@ -733,13 +955,14 @@ extern "C" qsa_status qsa_paged_mqa_logits(
   float* lg = static_cast<float*>(logits);
   fill_kernel<<<(unsigned)num_rows, 256, 0, st>>>(lg, logits_stride0, ctx, (int)next_n,
                                                   max_model_len);
-  const int stage_raw = (int)(kTile * kDim + N * kDim + kTile * 4 + N * 4);
-  const int stage_bytes = (stage_raw + 1023) & ~1023;
-  const int stages =
-      (int)std::min<int64_t>(kMaxStages, (int64_t)(kLogitSmem - 1024 - kMiscBytes - kTablesBytes) /
-                                             stage_bytes);
+  const int stage_bytes = (kTile * kDim + kTile * 4 + 1023) & ~1023;
+  const int qslot_bytes = (int)((N * kDim + N * 4 + 1023) & ~1023);
+  const int stages = (int)std::min<int64_t>(
+      kMaxStages,
+      (int64_t)(kLogitSmem - 1024 - 2 * qslot_bytes - kMiscBytes - kTablesBytes) / stage_bytes);
+  const int nacc = N <= 128 ? 4 : 2;       // accumulators of N fp32 columns in 512
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * N)) cols <<= 1;
+  while (cols < (uint32_t)(nacc * N)) cols <<= 1;
   const int64_t tiles_per_req = (max_model_len + kTile - 1) / kTile;
   for (int64_t b0 = 0; b0 < batch; b0 += kMaxBatch) {
     const int nb = (int)std::min<int64_t>(kMaxBatch, batch - b0);
@@ -763,6 +986,9 @@ extern "C" qsa_status qsa_paged_mqa_logits(
     p.qrow0 = (int)(b0 * N);
     p.stage_bytes = stage_bytes;
     p.stages = stages;
+    p.qslot_bytes = qslot_bytes;
+    p.nacc = nacc;
+    p.bs_log2 = __builtin_ctzll((unsigned long long)block_size);
     p.tmem_cols = cols;
     const int64_t items = (int64_t)nb * tiles_per_req;
     const int grid = (int)std::min<int64_t>(items, di->sms);
