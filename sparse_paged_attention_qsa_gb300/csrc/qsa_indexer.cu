@@ -11,20 +11,25 @@
 //   warp 0  producer: per 128-token tile of one request, each lane loads one
 //           of the tile's cache blocks -- a TMA of its 128-byte value rows
 //           (128-byte swizzle) and a bulk copy of its scales -- into a ring
-//           of shared-memory stages, the block ids fetched a tile ahead;
-//           the request's query rows (all heads of its next_n tokens, same
+//           of shared-memory stages; the warp arms up to four tiles per
+//           iteration from a warp-wide chunk of block-table entries; the
+//           request's query rows (all heads of its next_n tokens, same
 //           swizzle) and head weights go to one of two query slots once per
 //           request the CTA works on;
-//   warp 1  one lane issues four tcgen05.mma kind::f8f6f4 (M = 128 tokens,
-//           N = next_n x heads, K = 32 each) per tile into one of four TMEM
-//           accumulators (two when N = 256), then commits to the accumulator's and the stage's
-//           barriers; the warp owns the TMEM allocation;
-//   warps 2-9  epilogue in two groups of four warps (one warp per TMEM lane
-//           quarter) taking alternate tiles: each thread owns one token (its
-//           TMEM lane), reads its accumulator row with one tcgen05.ld per 64
-//           columns, forms sum_h w_h * ReLU(d_h) for every query row in fp32
-//           (packed pairs), scales, and writes the logits (consecutive
-//           threads, consecutive columns).
+//   warps 1, 18  MMA issuers, alternate tiles each: one lane issues four
+//           tcgen05.mma kind::f8f6f4 (M = 128 tokens, N = next_n x heads,
+//           K = 32 each) per tile into a TMEM accumulator of its own
+//           (tile n uses accumulator n % 4, or n % 2 when N = 256), commits
+//           to the accumulator's barrier, and refills nothing until that
+//           accumulator's previous tile is consumed -- then releases that
+//           tile's stage to the producer; warp 1 owns the TMEM allocation;
+//   warps 2-17  epilogue in four groups of four warps (one warp per TMEM
+//           lane quarter); group g takes the tiles of accumulator g, so no
+//           warp waits on a barrier phase ahead of its predecessor: each
+//           thread owns one token (its TMEM lane), reads its accumulator row
+//           with one tcgen05.ld per 64 columns, forms sum_h w_h * ReLU(d_h)
+//           for every query row in fp32 (packed pairs), scales, and writes
+//           the logits (consecutive threads, consecutive columns).
 // fill_kernel    writes -inf to each row's columns [L_r, max_model_len).
 // topk_rows_kernel  one CTA per row: exact radix select (11/11/10 bits) of
 //           the k-th largest ordered logit, emission of the larger ones and
@@ -53,7 +58,7 @@ constexpr int kDim = QSA_IDX_HEAD_DIM;      // 128 E4M3 values per query head / 
 constexpr int kTile = 128;                  // tokens per tile (MMA M)
 constexpr int kMaxN = 256;                  // next_n x heads (MMA N)
 #ifndef QSA_IDX_EPI_GROUPS
-#define QSA_IDX_EPI_GROUPS 2
+#define QSA_IDX_EPI_GROUPS 4
 #endif
 // Epilogue groups taking tiles in turn.  A group always owns the same
 // accumulators (tile n uses accumulator n % NA and group n % G with G
@@ -61,7 +66,13 @@ constexpr int kMaxN = 256;                  // next_n x heads (MMA N)
 // the previous phase has completed.
 constexpr int kEpiGroups = QSA_IDX_EPI_GROUPS;
 constexpr int kEpiWarps = 4 * kEpiGroups;       // one warp per TMEM lane quarter per group
-constexpr int kLogitThreads = (2 + kEpiWarps) * 32;
+#ifndef QSA_IDX_ISSUERS
+#define QSA_IDX_ISSUERS 2
+#endif
+constexpr int kIssuers = QSA_IDX_ISSUERS;       // MMA issuer warps: 1 and 2+kEpiWarps.. (lane 0 each)
+constexpr int kLogitThreads = (1 + kIssuers + kEpiWarps) * 32;
+constexpr int kLogitRegs = kEpiGroups > 3 ? (kIssuers > 2 ? 80 : 96) : (kEpiGroups > 2 ? 128 : 168);
+constexpr int kHeadChunk = kLogitRegs < 96 ? 32 : 64;   // TMEM columns per load
 constexpr int kMaxBatch = 1024;             // requests per launch (tables in smem)
 constexpr int kMaxStages = 12;
 constexpr int kMaxAcc = 4;                  // TMEM accumulators (512 columns / N, at most 4)
@@ -245,12 +256,12 @@ __device__ __forceinline__ float head_sum_n(uint32_t taddr, const float* w, int 
   return (lo.x + lo.y) + (hi.x + hi.y);
 }
 
-// columns [c0, c0 + nc), nc in {16, 32, 64}
+// columns [c0, c0 + nc), nc in {16, 32, kHeadChunk}
 __device__ __forceinline__ float head_sum(uint32_t taddr, const float* w, int c0, int nc) {
   switch (nc) {
     case 16: return head_sum_n<16>(taddr, w, c0);
     case 32: return head_sum_n<32>(taddr, w, c0);
-    default: return head_sum_n<64>(taddr, w, c0);
+    default: return head_sum_n<kHeadChunk>(taddr, w, c0);
   }
 }
 
@@ -264,7 +275,7 @@ __device__ __forceinline__ int64_t row_len(int64_t ctx, int next_n, int j, int64
 
 // up to 5 warps share an SM sub-partition's 16K registers: cap the registers
 // so they fit
-__global__ void __maxnreg__(kEpiGroups > 3 ? 96 : (kEpiGroups > 2 ? 128 : 168))
+__global__ void __maxnreg__(kLogitRegs)
 logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -357,7 +368,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
   const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
   volatile int* abort_flag = &s_abort;
   volatile int64_t* end_tile = &s_end_tile;
-  int64_t issued = 0;    // producer: stages armed; MMA: tiles issued
+  int64_t issued = 0;    // producer: stages armed
+  int64_t last_issued = -1;  // MMA issuer: its last tile
   int segs = 0;          // producer: query slots loaded
 
   if (warp == 0) {
@@ -406,6 +418,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
           break;
         }
         if (lane == 0) {
+          *end_tile = issued;           // the first tile index past the range
           desc[s].b = -1;
           bar_arrive(bar_full + 8 * s);
         }
@@ -501,15 +514,19 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         i = 0;
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp >= 2 + kEpiWarps) {
+    // ---------------- MMA issuers ----------------
+    // two issuers take alternate tiles (issuer g: tiles g, g + 2, ...), each
+    // into its own accumulators (n % NA has the parity of n) for epilogue
+    // group g: two independent MMA -> epilogue pipelines behind one producer
+    const int g = warp == 1 ? 0 : warp - (1 + kEpiWarps);   // issuer index
+    const int I = kIssuers < NA ? kIssuers : NA;            // active issuers (divides NA)
+    if (lane == 0 && g < I) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
-      int s = 0, round = 0, a = 0, around = 0;         // ring and accumulator positions
+      int s = g, round = 0, a = g, around = 0;          // ring / accumulator position of tile n
       uint32_t held = 0;                                // stage of the tile in each accumulator (8 bits each)
       uint32_t seen_q = 0xffffffffu;                    // query slot and phase last waited for
-      for (;; ++issued, s = s + 1 == S ? 0 : s + 1, round += s == 0,
-              a = a + 1 == NA ? 0 : a + 1, around += a == 0) {
+      for (int64_t n = g;; n += I) {
         // accumulator a free again: the epilogue is done with the tile that
         // used it, so that tile's stage (values, scales) can be refilled
         if (around > 0) {
@@ -520,21 +537,23 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
           }
           bar_arrive(bar_empty + 8 * ((held >> (8 * a)) & 0xffu));
         }
-        if (!wait_phase(bar_full + 8 * s, (uint32_t)(round & 1))) {
+        // tile n's data, or the producer's end marker covering tile n
+        int state = test_wait(bar_full + 8 * s, (uint32_t)(round & 1)) ? 1 : 0;
+        const uint64_t t0 = gtime();
+        while (state == 0) {
+          if (try_wait(bar_full + 8 * s, (uint32_t)(round & 1), 1000u)) state = 1;
+          else if (n >= *end_tile || *abort_flag) state = 2;
+          else if (gtime() - t0 > kWaitNs) state = 3;
+        }
+        if (state == 3) {
           *abort_flag = 1;
           report(p.err, kErrTimeoutBit);
           break;
         }
+        if (state == 2 || *abort_flag) break;
         held = (held & ~(0xffu << (8 * a))) | ((uint32_t)s << (8 * a));
         const TileDesc d = desc[s];
-        if (d.b < 0) {                // end of range: tell both epilogue groups
-          // the other groups see the marker while they wait (see below)
-          *end_tile = issued;
-          bar_arrive(bar_accf + 8 * a);
-          ++issued;
-          break;
-        }
-        if (*abort_flag) break;
+        if (d.b < 0) break;                             // the end marker's stage
         const int qs = (int)(d.qinfo & 1u);
         if ((d.qinfo & 3u) != seen_q) {         // a new query slot: wait for its rows
           if (!wait_phase(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
@@ -553,6 +572,17 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         for (int k = 0; k < kDim / 32; ++k) tc_mma(dt, da + 2 * k, db + 2 * k, idesc, k);
         tc_commit(bar_accf + 8 * a);
         if (d.qinfo & 4u) tc_commit(bar_qempty + 8 * qs);
+        last_issued = n;
+        s += I;
+        if (s >= S) {
+          s -= S;
+          ++round;
+        }
+        a += I;
+        if (a >= NA) {
+          a -= NA;
+          ++around;
+        }
       }
     }
   } else {
@@ -615,7 +645,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       for (int j = 0; j < 4; ++j) {
         if (j < p.next_n) {
           float acc = 0.f;
-          for (int c = 0; c < H; c += 64) acc += head_sum(taddr, wts, j * H + c, H < 64 ? H : 64);
+          for (int c = 0; c < H; c += kHeadChunk)
+            acc += head_sum(taddr, wts, j * H + c, H < kHeadChunk ? H : kHeadChunk);
           out[j] = scale * acc;
         }
       }
@@ -655,8 +686,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       for (int g = segs > 2 ? segs - 2 : 0; g < segs; ++g)
         wait_phase(bar_qfull + 8 * (g & 1), (uint32_t)((g >> 1) & 1));
     }
-    if (warp == 1 && lane == 0 && issued > 0) {
-      const int64_t m = issued - 1;
+    if ((warp == 1 || warp >= 2 + kEpiWarps) && lane == 0 && last_issued >= 0) {
+      const int64_t m = last_issued;
       wait_phase(bar_accf + 8 * (int)(m % NA), (uint32_t)((m / NA) & 1));
     }
     __syncthreads();
