@@ -43,12 +43,13 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic_R256_L131072.json")
+SELECTION_SOURCES = ("qsa_select.cu", "qsa_device.cuh", "qsa_internal.h")
 
 
 def _selection_traffic(workload: int, rows: int):
     """DRAM bytes per selection launch from the committed ncu summary, or
-    None when the kernels changed since the capture (source hashes differ)
-    or the workload is not the one captured."""
+    None when the selection kernels changed since the capture (the hashes of
+    their sources differ) or the workload is not the one captured."""
     import hashlib
     try:
         with open(TRAFFIC_FILE) as f:
@@ -57,6 +58,8 @@ def _selection_traffic(workload: int, rows: int):
             return None
         csrc = os.path.join(ROOT, "sparse_paged_attention_qsa_gb300", "csrc")
         for name, digest in d["sources_sha256"].items():
+            if name not in SELECTION_SOURCES:     # the figure covers the selection kernels
+                continue
             with open(os.path.join(csrc, name), "rb") as f:
                 if hashlib.sha256(f.read()).hexdigest() != digest:
                     return None

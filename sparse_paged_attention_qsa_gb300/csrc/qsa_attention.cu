@@ -7,10 +7,11 @@
 // [R,2051] int32 with holes and duplicates; caller-owned output.
 //
 // Split-width flash decoding:
-//   attn_partial_kernel  grid (splits, R); each CTA takes kSplit consecutive
-//                        entries of one row's index list; each warp compacts
-//                        its 32 entries to the valid tokens and walks them 8
-//                        at a time (8 KiB of K/V in flight per warp).  Logits
+//   attn_partial_kernel  grid (splits, R); each CTA takes kSplit = 256
+//                        consecutive entries of one row's index list (a
+//                        2051-wide row: 9 CTAs); each warp compacts its 64
+//                        entries to the valid tokens and walks them 8 at a
+//                        time (8 KiB of K/V in flight per warp).  Logits
 //                        (mixed-precision FMA, fp16 operands, binary32
 //                        accumulation) are reduced with one warp
 //                        reduce-scatter per batch; the online softmax runs in
@@ -27,8 +28,12 @@
 namespace qsa {
 namespace {
 
-constexpr int kSplit = 128;          // index entries per CTA
-constexpr int kAttWarps = 4;         // 32 entries per warp
+#ifndef QSA_ATT_SPLIT
+#define QSA_ATT_SPLIT 256
+#endif
+constexpr int kSplit = QSA_ATT_SPLIT;  // index entries per CTA
+constexpr int kAttWarps = 4;
+constexpr int kWarpEntries = kSplit / kAttWarps;   // 32 or 64 entries per warp
 constexpr int kAttThreads = kAttWarps * 32;
 constexpr int kBatch = 8;            // tokens per warp step
 constexpr int kPartFloats = kAttHeads * 2 + kAttHeads * kAttDim;   // m[3], l[3], acc[3][256]
@@ -72,8 +77,12 @@ __device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane) {
 }
 
 // One CTA = kSplit consecutive entries of one row's index list; each warp
-// takes 32 of them, compacts the valid ones (holes and unmapped pages
-// dropped) and walks them kBatch tokens at a time.  Lane l owns dims
+// takes kSplit/4 of them, compacts the valid ones (holes and unmapped pages
+// dropped) and walks them kBatch tokens at a time.  256 entries per CTA
+// amortise the CTA's fixed costs -- the dependent index -> page-table -> K/V
+// loads before streaming and the merge after it -- over 8 batches per warp
+// (128 entries: 0.106 ms on 256 x 2048 rows, 256: 0.101, 512: 0.116 with
+// too few CTAs to fill the GPU evenly).  Lane l owns dims
 // [8l, 8l+8) of K and V, so a token's 1 KiB (K then V) is two coalesced
 // 512-byte warp loads; a batch keeps 8 KiB in flight per warp.  The 24 head
 // logits of a batch are reduced with one reduce-scatter, after which lane l
@@ -89,7 +98,7 @@ attn_partial_kernel(const AttentionParams p) {
 
   __shared__ float sm_m[kAttWarps][kAttHeads], sm_l[kAttWarps][kAttHeads];
   __shared__ float sm_acc[kAttWarps][kAttHeads][kAttDim];
-  __shared__ uint32_t sm_tok[kAttWarps][32];
+  __shared__ uint32_t sm_tok[kAttWarps][kWarpEntries];
 
   pdl_trigger();   // the combine kernel may be scheduled early (it waits)
   const int req = p.t2r[r];
@@ -107,27 +116,32 @@ attn_partial_kernel(const AttentionParams p) {
     }
   }
 
-  // resolve this lane's entry to a token (page*512 + slot) or a hole
-  const int64_t j = (int64_t)split * kSplit + warp * 32 + lane;
-  bool valid = false;
-  uint32_t tok = 0;
-  if (rok && j < p.width) {
-    const int32_t i = p.idx[(int64_t)r * p.idx_stride0 + j];
-    if (i >= 0) {
-      const int64_t col = i >> 9;
-      int32_t pg = -1;
-      if (col < p.pt_cols) pg = p.pt[(int64_t)req * p.pt_stride0 + col];
-      if (pg >= 0 && pg < p.num_pages) {
-        valid = true;
-        tok = (uint32_t)pg * kKvPageTokens + (uint32_t)(i & 511);
-      } else {
-        report(p.err, kErrKvPage);
+  // resolve this warp's entries to tokens (page*512 + slot), dropping holes,
+  // 32 at a time (one per lane), compacted in order
+  int nvalid = 0;
+#pragma unroll
+  for (int c = 0; c < kWarpEntries; c += 32) {
+    const int64_t j = (int64_t)split * kSplit + warp * kWarpEntries + c + lane;
+    bool valid = false;
+    uint32_t tok = 0;
+    if (rok && j < p.width) {
+      const int32_t i = p.idx[(int64_t)r * p.idx_stride0 + j];
+      if (i >= 0) {
+        const int64_t col = i >> 9;
+        int32_t pg = -1;
+        if (col < p.pt_cols) pg = p.pt[(int64_t)req * p.pt_stride0 + col];
+        if (pg >= 0 && pg < p.num_pages) {
+          valid = true;
+          tok = (uint32_t)pg * kKvPageTokens + (uint32_t)(i & 511);
+        } else {
+          report(p.err, kErrKvPage);
+        }
       }
     }
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    if (valid) sm_tok[warp][nvalid + __popc(vmask & ((1u << lane) - 1u))] = tok;
+    nvalid += __popc(vmask);
   }
-  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-  const int nvalid = __popc(vmask);
-  if (valid) sm_tok[warp][__popc(vmask & ((1u << lane) - 1u))] = tok;
   __syncwarp();
 
   const int hh = lane & 3;         // head of this lane's logit after the reduce
@@ -242,7 +256,7 @@ attn_partial_kernel(const AttentionParams p) {
   }
 }
 
-constexpr int kMaxSplits = (kOutWidth + kSplit - 1) / kSplit;   // 17
+constexpr int kMaxSplits = (kOutWidth + kSplit - 1) / kSplit;   // 9
 
 // One CTA per row: log-sum-exp merge of the row's split partials, FP16
 // round-to-nearest output; thread d handles dim d of every head.  The
