@@ -101,6 +101,8 @@ attn_partial_kernel(const AttentionParams p) {
   __shared__ uint32_t sm_tok[kAttWarps][kWarpEntries];
 
   pdl_trigger();   // the combine kernel may be scheduled early (it waits)
+  pdl_wait();      // launched as a dependent of the previous kernel (the selection's
+                   // top-k when called after it): its output is complete and visible
   const int req = p.t2r[r];
   const bool rok = req >= 0 && req < p.num_reqs;
   if (!rok && split == 0 && tid == 0) report(p.err, kErrRequest);
@@ -323,8 +325,10 @@ size_t attention_workspace_bytes(int64_t R, int64_t width) {
 cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
   dim3 grid((unsigned)p.nsplit, (unsigned)p.R);
-  attn_partial_kernel<<<grid, kAttThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent of whatever ran before on the stream: after the
+  // selection's top-k (which triggers at its start) the launch and CTA
+  // scheduling overlap the top-k's tail; the kernel waits before any read
+  cudaError_t e = launch_after(attn_partial_kernel, grid, dim3(kAttThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   return launch_after(attn_combine_kernel, dim3(p.R), dim3(kAttDim), 0, stream, p);
 }

@@ -31,10 +31,11 @@
 //           for every query row in fp32 (packed pairs), scales, and writes
 //           the logits (consecutive threads, consecutive columns).
 // fill_kernel    writes -inf to each row's columns [L_r, max_model_len).
-// topk_rows_kernel  one CTA per row: exact radix select (11/11/10 bits) of
-//           the k-th largest ordered logit, emission of the larger ones and
-//           of the first ties in column order, bitonic sort of the k
-//           (logit, column) pairs.
+// topk_rows_kernel  one CTA of 512 threads per row: exact radix select
+//           (11/11/10 bits) of the k-th largest ordered logit, emission of
+//           the larger ones and of the first ties in column order (warp
+//           segments ranked by one scan), bitonic sort of the k (logit,
+//           column) pairs.
 // Every mbarrier wait gives up after 1 s (QSA_DERR_TIMEOUT), drains what the
 // CTA has in flight, frees its TMEM and returns.
 #include "qsa.h"
@@ -711,8 +712,10 @@ __global__ void fill_kernel(float* logits, int64_t ld, const int32_t* ctx, int n
 
 // --- top-k per row -----------------------------------------------------------
 
-constexpr int kTkThreads = 1024;
+constexpr int kTkThreads = 512;            // 16 warps; two CTAs per SM
+constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkMax = QSA_IDX_MAX_TOPK;   // 2048
+constexpr int kTkUnroll = 8;               // logits loaded per lane before use
 
 struct TkParams {
   const float* logits;
@@ -728,7 +731,8 @@ struct TkShared {
   unsigned long long sel[kTkMax];
   uint32_t hist[2048];
   uint32_t wsum[32];
-  uint32_t digit, above, total;
+  uint32_t wties[kTkWarps];
+  uint32_t digit, above;
   int cnt_above;
 };
 
@@ -743,7 +747,7 @@ __device__ __forceinline__ uint32_t ordered(float f) {
 // above(d) counts the keys in digits above d.
 __device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = nb / kTkThreads;
+  const int per = nb / kTkThreads;            // 4 or 2 bins per thread
   uint32_t local = 0;
   for (int k = 0; k < per; ++k) local += sh.hist[tid * per + k];
   uint32_t suf = local;                       // inclusive suffix within the warp
@@ -755,7 +759,7 @@ __device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
   if (lane == 0) sh.wsum[warp] = suf;
   __syncthreads();
   uint32_t above = suf - local;               // keys in this warp's higher threads
-  for (int w2 = warp + 1; w2 < 32; ++w2) above += sh.wsum[w2];
+  for (int w2 = warp + 1; w2 < kTkWarps; ++w2) above += sh.wsum[w2];
   for (int k = per - 1; k >= 0; --k) {
     const uint32_t h = sh.hist[tid * per + k];
     if (above < need && need <= above + h) {
@@ -767,7 +771,13 @@ __device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTkThreads, 1) topk_rows_kernel(const TkParams p) {
+// One CTA per row.  Radix select of the K-th largest ordered key (11, 11
+// and 10 bits, eight independent loads per lane in flight);
+// then every warp owns a contiguous column segment: it counts its keys equal
+// to the threshold, one block-wide scan ranks the segments, and one pass in
+// column order emits the larger keys and the first `need` ties; a bitonic
+// sort orders the K (key, column) pairs.
+__global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams p) {
   extern __shared__ unsigned char tk_raw[];
   TkShared& sh = *reinterpret_cast<TkShared*>(tk_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -795,59 +805,89 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_rows_kernel(const TkParams
       const int nb = 1 << widths[ps];
       for (int i = tid; i < 2048; i += kTkThreads) sh.hist[i] = 0;
       __syncthreads();
-      for (int64_t t = tid; t < L; t += kTkThreads) {
-        const uint32_t k = ordered(row[t * p.s1]);
-        if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shifts[ps]) & (nb - 1)], 1u);
+      // kTkUnroll independent loads in flight per lane
+      for (int64_t b0 = (int64_t)warp * 32; b0 < L; b0 += (int64_t)kTkThreads * kTkUnroll) {
+        uint32_t kv[kTkUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+          const int64_t t = b0 + (int64_t)u * kTkThreads + lane;
+          kv[u] = t < L ? ordered(row[t * p.s1]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+          const int64_t t = b0 + (int64_t)u * kTkThreads + lane;
+          const uint32_t k = kv[u];
+          const bool in = t < L && (k & mask) == prefix;
+          const uint32_t bin = (k >> shifts[ps]) & (uint32_t)(nb - 1);
+          if (in) atomicAdd(&sh.hist[bin], 1u);
+        }
       }
       __syncthreads();
-      tk_find_digit(sh, nb < kTkThreads ? kTkThreads : nb, need);
+      tk_find_digit(sh, nb < 1024 ? 1024 : nb, need);
       prefix |= sh.digit << shifts[ps];
       mask |= (uint32_t)(nb - 1) << shifts[ps];
       need -= sh.above;
       __syncthreads();
     }
     const uint32_t T = prefix;                 // the K-th largest key; `need` ties kept
+    // warp segments of seg columns (a multiple of 32), in column order
+    const int64_t seg = ((L + kTkWarps - 1) / kTkWarps + 31) & ~(int64_t)31;
+    const int64_t s_lo = (int64_t)warp * seg;
+    const int64_t s_hi = s_lo + seg < L ? s_lo + seg : L;
+    uint32_t ties = 0;
+    for (int64_t b0 = s_lo + lane; b0 < s_hi; b0 += 32 * kTkUnroll) {
+      uint32_t kv[kTkUnroll];
+#pragma unroll
+      for (int u = 0; u < kTkUnroll; ++u) {
+        const int64_t t = b0 + 32 * u;
+        kv[u] = t < s_hi ? ordered(row[t * p.s1]) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kTkUnroll; ++u) ties += kv[u] == T && b0 + 32 * u < s_hi;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ties += __shfl_xor_sync(0xffffffffu, ties, o);
+    if (lane == 0) sh.wties[warp] = ties;
     if (tid == 0) sh.cnt_above = 0;
     __syncthreads();
-    uint32_t running = 0;
-    for (int64_t b0 = 0; b0 < L; b0 += kTkThreads) {
-      const int64_t t = b0 + tid;
-      const uint32_t k = t < L ? ordered(row[t * p.s1]) : 0u;
-      if (t < L && k > T) sh.sel[atomicAdd(&sh.cnt_above, 1)] = pair(k, t);
-      const bool tie = t < L && k == T;
-      const uint32_t bal = __ballot_sync(0xffffffffu, tie);
-      if (lane == 0) sh.wsum[warp] = __popc(bal);
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t v = sh.wsum[lane];
-        uint32_t incl = v;
+    uint32_t rank = 0;                         // ties in the segments before this warp's
+    for (int w2 = 0; w2 < warp; ++w2) rank += sh.wties[w2];
+    for (int64_t c0 = s_lo; c0 < s_hi; c0 += 32 * kTkUnroll) {
+      uint32_t kv[kTkUnroll];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        sh.wsum[lane] = incl - v;
-        if (lane == 31) sh.total = incl;
+      for (int u = 0; u < kTkUnroll; ++u) {
+        const int64_t t = c0 + 32 * u + lane;
+        kv[u] = t < s_hi ? ordered(row[t * p.s1]) : 0u;
       }
-      __syncthreads();
-      const uint32_t rank = running + sh.wsum[warp] + __popc(bal & ((1u << lane) - 1u));
-      if (tie && rank < need) sh.sel[(uint32_t)K - need + rank] = pair(k, t);
-      running += sh.total;
-      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kTkUnroll; ++u) {              // in column order
+        const int64_t t = c0 + 32 * u + lane;
+        const uint32_t k = kv[u];
+        if (t < s_hi && k > T) sh.sel[atomicAdd(&sh.cnt_above, 1)] = pair(k, t);
+        const bool tie = t < s_hi && k == T;
+        const uint32_t bal = __ballot_sync(0xffffffffu, tie);
+        const uint32_t rk = rank + __popc(bal & ((1u << lane) - 1u));
+        if (tie && rk < need) sh.sel[(uint32_t)K - need + rk] = pair(k, t);
+        rank += __popc(bal);
+      }
     }
   }
   for (int i = K + tid; i < kTkMax; i += kTkThreads) sh.sel[i] = 0ull;
   __syncthreads();
-  // bitonic sort, descending
+  // bitonic sort, descending; each thread takes two of the 1024 pairs per step
   for (int kk = 2; kk <= kTkMax; kk <<= 1) {
     for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      const int lo = ((tid & ~(jj - 1)) << 1) | (tid & (jj - 1));
-      const int hi = lo + jj;
-      const unsigned long long x = sh.sel[lo], y = sh.sel[hi];
-      const bool desc_order = (lo & kk) == 0;
-      if (desc_order ? (x < y) : (x > y)) {
-        sh.sel[lo] = y;
-        sh.sel[hi] = x;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pi = tid + h * kTkThreads;
+        const int lo = ((pi & ~(jj - 1)) << 1) | (pi & (jj - 1));
+        const int hi = lo + jj;
+        const unsigned long long x = sh.sel[lo], y = sh.sel[hi];
+        const bool desc_order = (lo & kk) == 0;
+        if (desc_order ? (x < y) : (x > y)) {
+          sh.sel[lo] = y;
+          sh.sel[hi] = x;
+        }
       }
       __syncthreads();
     }

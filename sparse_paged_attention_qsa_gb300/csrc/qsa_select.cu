@@ -714,6 +714,7 @@ topk_kernel(const SelectParams p) {
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();   // a dependent (the attention kernel) may be scheduled early (it waits)
   const RowSetup rs = row_setup(p, r);
   int32_t* out = p.out + (int64_t)r * p.out_stride0;
   if (!rs.ok) {
