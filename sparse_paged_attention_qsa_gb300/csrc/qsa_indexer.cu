@@ -31,11 +31,14 @@
 //           for every query row in fp32 (packed pairs), scales, and writes
 //           the logits (consecutive threads, consecutive columns).
 // fill_kernel    writes -inf to each row's columns [L_r, max_model_len).
-// topk_rows_kernel  one CTA of 512 threads per row: exact radix select
-//           (11/11/10 bits) of the k-th largest ordered logit, emission of
-//           the larger ones and of the first ties in column order (warp
-//           segments ranked by one scan), bitonic sort of the k (logit,
-//           column) pairs.
+// topk_rows_kernel  one CTA of 512 threads per row: a threshold from 8192
+//           sampled logits, one float4 pass keeping the logits at or above
+//           it (about 4096 of a long row) in shared memory, an exact radix
+//           select of the k-th largest there (digits spread over the
+//           candidates' range), emission of the larger ones and of the
+//           first ties in column order, bitonic sort of the k (logit,
+//           column) pairs.  A row whose candidates do not fit (or are too
+//           few) is selected with radix passes over the row itself.
 // Every mbarrier wait gives up after 1 s (QSA_DERR_TIMEOUT), drains what the
 // CTA has in flight, frees its TMEM and returns.
 #include "qsa.h"
@@ -715,7 +718,12 @@ __global__ void fill_kernel(float* logits, int64_t ld, const int32_t* ctx, int n
 constexpr int kTkThreads = 512;            // 16 warps; two CTAs per SM
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkMax = QSA_IDX_MAX_TOPK;   // 2048
-constexpr int kTkUnroll = 8;               // logits loaded per lane before use
+constexpr int kTkUnroll = 8;               // scalar logits loaded per lane before use
+constexpr int kTkVec = 4;                  // float4 loads per lane before use
+constexpr int kTkCand = 10240;             // candidate (key, column) pairs kept in smem
+constexpr int kTkChunks = 256;             // sampled 32-column chunks of a long row
+constexpr int kTkSample = kTkChunks * 32;  // 8192 sampled keys
+constexpr int kTkTarget = 4096;            // candidates the sampled threshold aims at
 
 struct TkParams {
   const float* logits;
@@ -730,10 +738,14 @@ struct TkParams {
 struct TkShared {
   unsigned long long sel[kTkMax];
   uint32_t hist[2048];
-  uint32_t wsum[32];
+  uint32_t cand_k[kTkCand];
+  uint32_t cand_i[kTkCand];
+  uint32_t wsum[kTkWarps];
+  uint32_t wmax[kTkWarps];
   uint32_t wties[kTkWarps];
-  uint32_t digit, above;
+  uint32_t digit, above, dcount;
   int cnt_above;
+  int ncand;
 };
 
 // Unsigned key with the order of the float (-0 taken as +0: they are equal).
@@ -743,8 +755,24 @@ __device__ __forceinline__ uint32_t ordered(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose key is k (k the key of some float; never -0).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Warp-wide: the lanes with c set take consecutive slots from *counter (one
+// shared atomic per warp); returns this lane's slot (meaningful where c).
+__device__ __forceinline__ int tk_warp_slot(int* counter, bool c) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t bal = __ballot_sync(0xffffffffu, c);
+  int base = 0;
+  if (lane == 0 && bal) base = atomicAdd(counter, __popc(bal));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  return base + __popc(bal & ((1u << lane) - 1u));
+}
+
 // hist[0..nb): the digit d with above(d) < need <= above(d) + hist[d], where
-// above(d) counts the keys in digits above d.
+// above(d) counts the keys in digits above d; also its count hist[d].
 __device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = nb / kTkThreads;            // 4 or 2 bins per thread
@@ -765,18 +793,85 @@ __device__ void tk_find_digit(TkShared& sh, int nb, uint32_t need) {
     if (above < need && need <= above + h) {
       sh.digit = (uint32_t)(tid * per + k);
       sh.above = above;
+      sh.dcount = h;
     }
     above += h;
   }
   __syncthreads();
 }
 
-// One CTA per row.  Radix select of the K-th largest ordered key (11, 11
-// and 10 bits, eight independent loads per lane in flight);
-// then every warp owns a contiguous column segment: it counts its keys equal
-// to the threshold, one block-wide scan ranks the segments, and one pass in
-// column order emits the larger keys and the first `need` ties; a bitonic
-// sort orders the K (key, column) pairs.
+// The K-th largest of the smem keys x[0..n) (1 <= K <= n): a radix select
+// over x - min(x), 11-bit digits from the top set bit of max(x) - min(x)
+// down, so the first digit spreads the keys over the range they really
+// span.  *need = how many keys equal to it are among the K largest,
+// *tcount = how many keys equal it.  Ends on a block barrier after its last
+// read of x.
+__device__ uint32_t tk_select(TkShared& sh, const uint32_t* x, int n, uint32_t K,
+                              uint32_t* need_out, uint32_t* tcount_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += kTkThreads) {
+    const uint32_t k = x[i];
+    lo = min(lo, k);
+    hi = max(hi, k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    sh.wsum[warp] = lo;
+    sh.wmax[warp] = hi;
+  }
+  __syncthreads();
+  lo = sh.wsum[0];
+  hi = sh.wmax[0];
+  for (int w2 = 1; w2 < kTkWarps; ++w2) {
+    lo = min(lo, sh.wsum[w2]);
+    hi = max(hi, sh.wmax[w2]);
+  }
+  __syncthreads();
+  const uint32_t range = hi - lo;
+  int shift = range ? 32 - __clz(range) : 0;
+  uint32_t prefix = 0, need = K, tcount = (uint32_t)n;
+  while (shift > 0) {
+    const int w = shift < 11 ? shift : 11;
+    shift -= w;
+    const uint32_t himask = shift + w >= 32 ? 0u : (0xFFFFFFFFu << (shift + w));
+    const uint32_t dmask = (1u << w) - 1u;
+    for (int i = tid; i < 2048; i += kTkThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kTkThreads) {
+      const uint32_t rel = x[i] - lo;
+      if ((rel & himask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    tk_find_digit(sh, w <= 10 ? 1024 : 2048, need);
+    prefix |= sh.digit << shift;
+    need -= sh.above;
+    tcount = sh.dcount;
+    __syncthreads();
+  }
+  *need_out = need;
+  *tcount_out = tcount;
+  return lo + prefix;
+}
+
+// One CTA per row.
+//  * L <= 10240: the whole row's (key, column) pairs go to shared memory.
+//  * longer rows: 256 chunks of 32 columns spread over the row are sampled;
+//    their ceil(4096 * 8192 / L)-th largest key T0 is a threshold about 4096
+//    of the row's keys reach.  One pass (float4 loads where the row allows)
+//    keeps the keys >= T0.  When between K and 10240 keys qualify, the K
+//    largest of the row are among them; otherwise (a skewed sample, or
+//    heavy ties) the row takes three radix passes over global memory
+//    instead (11/11/10 bits) and an emission pass in warp segments ranked
+//    by one scan.
+// The exact K-th largest key T is selected in shared memory; the keys above
+// it and the `need` ties with the smallest columns (a second select, over
+// the ties' columns, only when not every tie is kept) are emitted, and a
+// bitonic sort orders the K (key, column) pairs.
 __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams p) {
   extern __shared__ unsigned char tk_raw[];
   TkShared& sh = *reinterpret_cast<TkShared*>(tk_raw);
@@ -795,9 +890,127 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams
   const auto pair = [](uint32_t key, int64_t t) {
     return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
   };
-  if (L <= p.topk) {
-    for (int64_t t = tid; t < L; t += kTkThreads) sh.sel[t] = pair(ordered(row[t * p.s1]), t);
+  int n;
+  if (L <= kTkCand) {
+    for (int t = tid; t < (int)L; t += kTkThreads) {
+      sh.cand_k[t] = ordered(row[(int64_t)t * p.s1]);
+      sh.cand_i[t] = (uint32_t)t;
+    }
+    n = (int)L;
+    __syncthreads();
   } else {
+    const int64_t stride = L / kTkChunks;               // >= 40 columns
+#pragma unroll 4
+    for (int c = warp; c < kTkChunks; c += kTkWarps)
+      sh.cand_k[c * 32 + lane] = ordered(row[((int64_t)c * stride + lane) * p.s1]);
+    __syncthreads();
+    const uint32_t q = (uint32_t)(((int64_t)kTkTarget * kTkSample + L - 1) / L);   // 1..4096
+    uint32_t dn, dc;
+    const float f0 = key_float(tk_select(sh, sh.cand_k, kTkSample, q, &dn, &dc));
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    if (p.s1 == 1 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0 && L < (1ll << 31)) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const int n4 = (int)(L >> 2);
+      for (int b = warp * 32; b < n4; b += kTkThreads * kTkVec) {
+        float4 v[kTkVec];
+#pragma unroll
+        for (int u = 0; u < kTkVec; ++u) {
+          const int i = b + u * kTkThreads + lane;
+          v[u] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        uint32_t bal[kTkVec][4];
+        int tot = 0;
+#pragma unroll
+        for (int u = 0; u < kTkVec; ++u) {
+          const bool in = b + u * kTkThreads + lane < n4;
+          bal[u][0] = __ballot_sync(0xffffffffu, in && v[u].x >= f0);
+          bal[u][1] = __ballot_sync(0xffffffffu, in && v[u].y >= f0);
+          bal[u][2] = __ballot_sync(0xffffffffu, in && v[u].z >= f0);
+          bal[u][3] = __ballot_sync(0xffffffffu, in && v[u].w >= f0);
+          tot += __popc(bal[u][0]) + __popc(bal[u][1]) + __popc(bal[u][2]) + __popc(bal[u][3]);
+        }
+        if (tot == 0) continue;                          // warp-uniform
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sh.ncand, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int u = 0; u < kTkVec; ++u) {
+          const uint32_t col = 4u * (uint32_t)(b + u * kTkThreads + lane);
+          const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int slot = base + __popc(bal[u][j] & below);
+            if (((bal[u][j] >> lane) & 1u) && slot < kTkCand) {
+              sh.cand_k[slot] = ordered(f[j]);
+              sh.cand_i[slot] = col + (uint32_t)j;
+            }
+            base += __popc(bal[u][j]);
+          }
+        }
+      }
+      const int t = 4 * n4 + tid;                        // the last L % 4 columns
+      if (t < L && row[t] >= f0) {
+        const int slot = atomicAdd(&sh.ncand, 1);
+        if (slot < kTkCand) {
+          sh.cand_k[slot] = ordered(row[t]);
+          sh.cand_i[slot] = (uint32_t)t;
+        }
+      }
+    } else {
+      for (int64_t b0 = (int64_t)warp * 32; b0 < L; b0 += (int64_t)kTkThreads * kTkUnroll) {
+        float f[kTkUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+          const int64_t t = b0 + (int64_t)u * kTkThreads + lane;
+          f[u] = t < L ? row[t * p.s1] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+          const int64_t t = b0 + (int64_t)u * kTkThreads + lane;
+          const bool c = t < L && f[u] >= f0;
+          const int slot = tk_warp_slot(&sh.ncand, c);
+          if (c && slot < kTkCand) {
+            sh.cand_k[slot] = ordered(f[u]);
+            sh.cand_i[slot] = (uint32_t)t;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    n = sh.ncand;
+  }
+  if (n >= K && n <= kTkCand) {
+    uint32_t need, tcount;
+    const uint32_t T = tk_select(sh, sh.cand_k, n, (uint32_t)K, &need, &tcount);
+    const bool all_ties = need == tcount;
+    if (tid == 0) sh.cnt_above = 0;
+    __syncthreads();
+    for (int i0 = warp * 32; i0 < n; i0 += kTkThreads) {
+      const int i = i0 + lane;
+      const uint32_t k = i < n ? sh.cand_k[i] : 0u;
+      const uint32_t col = i < n ? sh.cand_i[i] : 0u;
+      const bool c = i < n && (k > T || (all_ties && k == T));
+      const int slot = tk_warp_slot(&sh.cnt_above, c);
+      if (c) sh.sel[slot] = pair(k, col);
+      // for the column select: a tie's key becomes 2^32-1 - column (> 0,
+      // columns being < 2^31), every other key 0
+      if (!all_ties && i < n) sh.cand_k[i] = k == T ? 0xFFFFFFFFu - col : 0u;
+    }
+    if (!all_ties) {                                     // block-uniform
+      __syncthreads();
+      uint32_t cn, cc;
+      const uint32_t C = tk_select(sh, sh.cand_k, n, need, &cn, &cc);   // the need-th smallest tie column
+      for (int i0 = warp * 32; i0 < n; i0 += kTkThreads) {
+        const int i = i0 + lane;
+        const uint32_t kc = i < n ? sh.cand_k[i] : 0u;
+        const bool c = kc != 0u && kc >= C;
+        const int slot = tk_warp_slot(&sh.cnt_above, c);
+        if (c) sh.sel[slot] = pair(T, 0xFFFFFFFFu - kc);
+      }
+    }
+  } else {                                      // select over the row in global memory
     uint32_t prefix = 0, mask = 0, need = (uint32_t)K;
     const int shifts[3] = {21, 10, 0};
     const int widths[3] = {11, 11, 10};
@@ -805,7 +1018,6 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams
       const int nb = 1 << widths[ps];
       for (int i = tid; i < 2048; i += kTkThreads) sh.hist[i] = 0;
       __syncthreads();
-      // kTkUnroll independent loads in flight per lane
       for (int64_t b0 = (int64_t)warp * 32; b0 < L; b0 += (int64_t)kTkThreads * kTkUnroll) {
         uint32_t kv[kTkUnroll];
 #pragma unroll
@@ -817,9 +1029,8 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams
         for (int u = 0; u < kTkUnroll; ++u) {
           const int64_t t = b0 + (int64_t)u * kTkThreads + lane;
           const uint32_t k = kv[u];
-          const bool in = t < L && (k & mask) == prefix;
-          const uint32_t bin = (k >> shifts[ps]) & (uint32_t)(nb - 1);
-          if (in) atomicAdd(&sh.hist[bin], 1u);
+          if (t < L && (k & mask) == prefix)
+            atomicAdd(&sh.hist[(k >> shifts[ps]) & (uint32_t)(nb - 1)], 1u);
         }
       }
       __syncthreads();
@@ -863,7 +1074,9 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams
       for (int u = 0; u < kTkUnroll; ++u) {              // in column order
         const int64_t t = c0 + 32 * u + lane;
         const uint32_t k = kv[u];
-        if (t < s_hi && k > T) sh.sel[atomicAdd(&sh.cnt_above, 1)] = pair(k, t);
+        const bool above = t < s_hi && k > T;
+        const int slot = tk_warp_slot(&sh.cnt_above, above);
+        if (above) sh.sel[slot] = pair(k, t);
         const bool tie = t < s_hi && k == T;
         const uint32_t bal = __ballot_sync(0xffffffffu, tie);
         const uint32_t rk = rank + __popc(bal & ((1u << lane) - 1u));
@@ -872,14 +1085,14 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_rows_kernel(const TkParams
       }
     }
   }
-  for (int i = K + tid; i < kTkMax; i += kTkThreads) sh.sel[i] = 0ull;
+  // bitonic sort, descending, over the next power of two >= K
+  int size = 64;
+  while (size < K) size <<= 1;
+  for (int i = K + tid; i < size; i += kTkThreads) sh.sel[i] = 0ull;
   __syncthreads();
-  // bitonic sort, descending; each thread takes two of the 1024 pairs per step
-  for (int kk = 2; kk <= kTkMax; kk <<= 1) {
+  for (int kk = 2; kk <= size; kk <<= 1) {
     for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int pi = tid + h * kTkThreads;
+      for (int pi = tid; pi < (size >> 1); pi += kTkThreads) {
         const int lo = ((pi & ~(jj - 1)) << 1) | (pi & (jj - 1));
         const int hi = lo + jj;
         const unsigned long long x = sh.sel[lo], y = sh.sel[hi];

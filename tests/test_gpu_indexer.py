@@ -148,7 +148,10 @@ def test_topk_on_tied_indexer_logits():
 
 
 @pytest.mark.parametrize("distinct,cols,topk", [(0, 70000, 2048), (3, 10000, 2048), (1, 5000, 100),
-                                                (50, 4096, 2048), (0, 2100, 2048)])
+                                                (50, 4096, 2048), (0, 2100, 2048),
+                                                # heavy ties on long rows: more candidates than the
+                                                # kernel keeps on chip (its fallback path)
+                                                (2, 30000, 2048), (1, 12000, 64), (0, 131072, 1)])
 def test_topk_synthetic_rows(distinct, cols, topk):
     g = torch.Generator(device=DEV).manual_seed(distinct + cols)
     rows, next_n = 6, 3
@@ -171,3 +174,26 @@ def test_topk_strided_columns_and_short_rows():
     seq = torch.tensor([3000, 10, 1, 2500], dtype=torch.int32, device=DEV)
     _check_topk(view, 1, seq, 2048)
     _check_topk(view, 1, seq, 5)
+
+
+def test_topk_sample_skew_and_alignment():
+    # Rows built against the kernel's sampled threshold (32-column chunks at
+    # multiples of L // 256): large logits exactly on the sampled chunks
+    # (too few candidates), large logits only between them (too many), an
+    # increasing row, and a row whose start is not 16-byte aligned.
+    L = 65536
+    g = torch.Generator(device=DEV).manual_seed(21)
+    lg = torch.randn(5, L + 3, device=DEV, generator=g) * 0.01
+    stride = L // 256
+    cols = (torch.arange(256, device=DEV)[:, None] * stride + torch.arange(32, device=DEV)).flatten()
+    lg[0, cols] += 10.0
+    off = torch.ones(L + 3, dtype=torch.bool, device=DEV)
+    off[cols] = False
+    lg[1, off] += 10.0
+    lg[2] = torch.arange(L + 3, device=DEV, dtype=torch.float32) * 1e-3
+    seq = torch.full((5,), L, dtype=torch.int32, device=DEV)
+    _check_topk(lg[:, :L], 1, seq, 2048)                  # row stride L + 3: rows 1.. misaligned
+    _check_topk(lg[:, :L].contiguous(), 1, seq, 2048)
+    seq_t = torch.tensor([L - 1, L - 2, L - 3, 40000, 10241], dtype=torch.int32, device=DEV)
+    _check_topk(lg[:, :L].contiguous(), 1, seq_t, 2048)   # float4 tails of 1..3 columns
+    _check_topk(lg[:, :L].contiguous(), 1, seq_t, 3)
