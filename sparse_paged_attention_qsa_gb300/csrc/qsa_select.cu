@@ -13,9 +13,11 @@
 //                 shared memory (the dominant HBM stream: 256 B per key) and
 //                 writes a 32-bit ordered score key per block to the
 //                 workspace;
-//   topk_kernel   one CTA per row: exact radix select of the top-512 keys over
-//                 the row's scores (L2-resident), bitonic sort of the winners,
-//                 expansion, tail and -1 padding.
+//   topk_kernel   one CTA per row: a lower bound of the 512-th largest key
+//                 from the per-thread maxima of one sweep, the keys reaching
+//                 it as candidates (a second sweep), exact radix select of
+//                 the top 512 over them, ordering of the winners, expansion,
+//                 tail and -1 padding.
 //
 // Score arithmetic (must match the oracle bit for bit): per head, four
 // 32-dim slices; in each slice an even-dim and an odd-dim binary32 chain
@@ -570,48 +572,76 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 // ---------------------------------------------------------------------------
 //
 // One CTA per row.  Keys are bits(score)+1 (bit 31 clear, 0 = no key).
-//  1. One sweep counts the keys and takes each thread's maximum.  If at least
-//     K = min(512, #keys) threads hold a key, the smallest of those maxima is
-//     a lower bound L0 of the K-th largest key (at least K distinct keys --
-//     the maxima -- are >= it); otherwise L0 = 1.
-//  2. A second sweep appends every key >= L0 (with its block index) to a
-//     candidate list in shared memory: about 9 % of a 32768-key row.
-//  3. MSB-first radix select over the candidates (digits 30..20, 19..9,
-//     8..0) finds T, the K-th largest key, and `need`, how many keys equal
-//     to T belong to the top K.  If more than `need` keys equal T, a second
-//     radix select over (2^31-1 - block index) of those ties keeps the
-//     `need` smallest block indices (the tie rule).
-//  4. The K (key, ~index) pairs are ordered (warp sorts + rank merge),
+//  1. One sweep (16-byte loads, eight in flight per thread) counts the keys
+//     and takes each thread's maximum and the row's maximum M; a row of at
+//     most 8192 blocks also keeps every key, with its block index, as a
+//     candidate in shared memory (one shared atomic per warp and step).
+//  2. A longer row: if at least K = min(512, #keys) threads hold a key, the
+//     smallest of their maxima is a lower bound L0 of the K-th largest key
+//     (K distinct keys -- the maxima -- are >= it), else L0 = 1; a second
+//     sweep keeps the keys >= L0 (about 9 % of a 32768-key row).
+//  3. Radix select over the candidates' offsets from their lower bound finds
+//     T, the K-th largest key, and `need`, how many keys equal to T belong to
+//     the top K.
+//     If more than `need` keys equal T, a second select over (2^31-1 - block
+//     index) of those ties keeps the `need` smallest block indices (the tie
+//     rule).
+//  4. The K (key, ~index) pairs are ordered (a bitonic sort of 512 slots),
 //     expanded, tail appended.
-// A row whose candidates overflow the list falls back to radix passes over
-// all of its keys, re-read from the workspace (L2).
+// Every select takes 12-bit digits of (x - lo) from the top bit of hi - lo
+// down, so its first digit already spreads the members over the range they
+// span, and stops at the first digit whose bin holds exactly the members
+// still needed.  A row whose candidates still overflow the list falls back
+// to the same select over all of its keys, re-read from the workspace.
 
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kCandCap = 8192;
-constexpr int kWarpCand = kCandCap / kTopkWarps;        // 512 slots per warp region
-constexpr int kSweepUnroll = 8;
+constexpr int kCandCap = 8192;                          // candidate (key, block) pairs
+constexpr int kSweepVec = 8;                            // 16-byte loads in flight per thread
+constexpr int kDigitBits = 12;
+constexpr int kBins = 1 << kDigitBits;                  // 4096 histogram bins
+constexpr int kBinsPerThread = kBins / kTopkThreads;    // 8
 
 struct TopkShared {
-  uint32_t hist[2048];
+  uint32_t hist[kBins];
   unsigned long long keys[kTopkBlocks];
   uint32_t cand_x[kCandCap];
   uint32_t cand_i[kCandCap];
   uint32_t wsum[kTopkWarps];
-  uint32_t wmin[kTopkWarps];
   uint32_t wcnt[kTopkWarps];
-  uint32_t wcand[kTopkWarps];      // candidates in each warp's region
+  uint32_t wmin[kTopkWarps];
+  uint32_t wmax[kTopkWarps];
   uint32_t found_digit, found_above;
-  int count;
+  int count;                       // kept pairs in keys[]
+  int ncand;
 };
 constexpr size_t kTopkSmem = sizeof(TopkShared);
 
+// Score keys are written by another kernel; read them from L2 (not through
+// the non-coherent path), 16 bytes at a time.
+__device__ __forceinline__ uint4 ld_cg16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
+  return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
+
 // Suffix scan of the histogram: find the digit d with
 // above(d) < need <= above(d) + hist[d]; returns d and above(d).
-__device__ __forceinline__ void find_digit(TopkShared& sh, int nbins, uint32_t need, int tid,
-                                           int lane, int warp) {
-  const int per = nbins / kTopkThreads;          // 4 or 1 bins per thread
+__device__ __forceinline__ void find_digit(TopkShared& sh, uint32_t need, int tid, int lane,
+                                           int warp) {
+  uint32_t h[kBinsPerThread];
   uint32_t local = 0;
-  for (int b = 0; b < per; ++b) local += sh.hist[tid * per + b];
+#pragma unroll
+  for (int b = 0; b < kBinsPerThread; ++b) {
+    h[b] = sh.hist[tid * kBinsPerThread + b];
+    local += h[b];
+  }
   uint32_t suf = local;                           // inclusive suffix within the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -623,83 +653,107 @@ __device__ __forceinline__ void find_digit(TopkShared& sh, int nbins, uint32_t n
   uint32_t higher = 0;
   for (int w = warp + 1; w < kTopkWarps; ++w) higher += sh.wsum[w];
   uint32_t above = higher + suf - local;          // keys in bins above this thread's
-  if (need > 0 && above < need && above + local >= need) {
-    for (int b = per - 1; b >= 0; --b) {
-      const uint32_t h = sh.hist[tid * per + b];
-      if (above + h >= need) {
-        sh.found_digit = (uint32_t)(tid * per + b);
+  if (above < need && above + local >= need) {
+#pragma unroll
+    for (int b = kBinsPerThread - 1; b >= 0; --b) {
+      if (above < need && above + h[b] >= need) {
+        sh.found_digit = (uint32_t)(tid * kBinsPerThread + b);
         sh.found_above = above;
-        break;
       }
-      above += h;
+      above += h[b];
     }
   }
   __syncthreads();
 }
 
-// Radix select over n items: item_key gives item c's key (< 2^31; 0 = not a
-// member).  Returns T, the k-th largest member key, `need` (how many members
-// equal to T are in the top k) and the number of members equal to T.
+// Radix select result.  Exactly `need` of the members equal to T are among
+// the k largest and every member above T is; `clean` means that the k
+// largest are exactly the members >= T (T may then lie below the k-th
+// largest member, at the low end of its digit).
 struct Selected {
-  uint32_t T, need, eq_total;
+  uint32_t T, need;
+  bool clean;
 };
 
-// item keys for radix_select: the candidate list or all of the row's keys,
-// either as is or as (2^31-1 - block index) of the ties equal to T
-enum KeyMode { kCand = 0, kCandTie = 1, kRow = 2, kRowTie = 3 };
-
-template <int Mode>
-__device__ __forceinline__ uint32_t item_key(const TopkShared& sh, const uint32_t* sc, int64_t c,
+// Members of a select are the nonzero src[c], c in [0, n) -- a row's keys
+// or the candidate keys -- or, for a tie select, the items
+// equal to T mapped to (2^31-1 - block index), the block index being c, or
+// cand_i[c] for candidates.
+template <bool kTie, bool kCandIdx>
+__device__ __forceinline__ uint32_t item_key(const TopkShared& sh, const uint32_t* src, int64_t c,
                                              uint32_t T) {
-  if (Mode == kCand || Mode == kCandTie) {
-    if ((uint32_t)(c % kWarpCand) >= sh.wcand[c / kWarpCand]) return 0u;   // empty slot
-    if (Mode == kCand) return sh.cand_x[c];
-    return sh.cand_x[c] == T ? 0x7fffffffu - sh.cand_i[c] : 0u;
-  }
-  if (Mode == kRow) return sc[c];
-  return sc[c] == T ? 0x7fffffffu - (uint32_t)c : 0u;
+  const uint32_t x = src[c];
+  if (!kTie) return x;
+  return x == T ? 0x7fffffffu - (kCandIdx ? sh.cand_i[c] : (uint32_t)c) : 0u;
 }
 
-template <int Mode>
-__device__ __forceinline__ Selected radix_select(TopkShared& sh, const uint32_t* sc, int64_t n,
-                                                 uint32_t k, uint32_t T = 0) {
+// Every member lies in [lo, hi].  Digits of (x - lo) are taken kDigitBits at
+// a time from the top set bit of hi - lo down.  The select stops as soon as
+// the bin of the k-th largest member holds exactly the members still needed
+// (then every member >= lo + prefix is in the top k: `clean`), after
+// `max_passes` passes (T is then a lower bound of the k-th largest member:
+// at least k members are >= T), or at the last digit, where T is exact.
+template <bool kTie, bool kCandIdx>
+__device__ Selected radix_select(TopkShared& sh, const uint32_t* src, int64_t n, uint32_t k,
+                                 uint32_t lo, uint32_t hi, uint32_t T = 0, int max_passes = 3) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, pmask = 0, need = k;
+  int shift = 32 - __clz((hi - lo) | 1u);          // bits still to resolve (>= 1)
+  uint32_t prefix = 0, need = k;
+  bool clean = false;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 20 : (pass == 1 ? 9 : 0);   // digits 30..20, 19..9, 8..0
-    const int nbins = pass == 2 ? 512 : 2048;
-    const uint32_t dmask = (uint32_t)nbins - 1u;
-    for (int i = tid; i < nbins; i += kTopkThreads) sh.hist[i] = 0;
+  for (int pass = 0; shift > 0 && pass < max_passes && !clean; ++pass) {
+    const int w = shift < kDigitBits ? shift : kDigitBits;
+    shift -= w;
+    const uint32_t himask = shift + w >= 32 ? 0u : (0xffffffffu << (shift + w));
+    const uint32_t dmask = (1u << w) - 1u;
+    for (int i = tid; i < kBins; i += kTopkThreads) sh.hist[i] = 0;
     __syncthreads();
     for (int64_t c = tid; c < n; c += kTopkThreads) {
-      const uint32_t x = item_key<Mode>(sh, sc, c, T);
-      if (x != 0u && (x & pmask) == prefix) atomicAdd(&sh.hist[(x >> shift) & dmask], 1u);
+      const uint32_t x = item_key<kTie, kCandIdx>(sh, src, c, T);
+      const uint32_t rel = x - lo;
+      if (x != 0u && (rel & himask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
     }
     __syncthreads();
-    find_digit(sh, nbins, need, tid, lane, warp);
+    find_digit(sh, need, tid, lane, warp);
     prefix |= sh.found_digit << shift;
-    pmask |= dmask << shift;
     need -= sh.found_above;
+    clean = sh.hist[sh.found_digit] == need;
     __syncthreads();
   }
-  Selected r{prefix, need, sh.hist[prefix & 511u]};   // last pass: one bin per key value
-  __syncthreads();
-  return r;
+  return Selected{lo + prefix, need, clean};
 }
 
-// Append (key, ~index) for the lanes with `take`; one shared atomic per warp.
-// Every lane of the warp must call this together.
+// Warp-wide: the lanes with `take` get consecutive slots from *counter (one
+// shared atomic per warp); returns this lane's slot (meaningful where take).
+__device__ __forceinline__ int warp_slot(int* counter, bool take, int lane) {
+  const unsigned bal = __ballot_sync(0xffffffffu, take);
+  int base = 0;
+  if (lane == 0 && bal) base = atomicAdd(counter, __popc(bal));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  return base + __popc(bal & ((1u << lane) - 1u));
+}
+
+// Warp-wide: reserve `cnt` consecutive slots of *counter for each lane (one
+// shared atomic per warp); returns this lane's first slot.
+__device__ __forceinline__ int warp_reserve(int* counter, int cnt, int lane) {
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int base = 0;
+  if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
+  base = __shfl_sync(0xffffffffu, base, 31);
+  return base + incl - cnt;
+}
+
+// Append (key, ~index) for the lanes with `take`.  Every lane of the warp
+// must call this together.
 __device__ __forceinline__ void emit_warp(TopkShared& sh, bool take, uint32_t x, int64_t idx,
                                           int lane) {
-  const unsigned bal = __ballot_sync(0xffffffffu, take);
-  if (!bal) return;
-  int base = 0;
-  if (lane == 0) base = atomicAdd(&sh.count, __popc(bal));
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (take)
-    sh.keys[base + __popc(bal & ((1u << lane) - 1u))] =
-        ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
+  const int slot = warp_slot(&sh.count, take, lane);
+  if (take) sh.keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
 }
 
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
@@ -725,107 +779,140 @@ topk_kernel(const SelectParams p) {
   }
   if (tid == 0 && rs.V > p.vcap) report(p.err, kErrCmpPage);
   const int64_t Vs = rs.V < p.vcap ? rs.V : p.vcap;
-  const uint32_t* sc = p.scores + (int64_t)r * p.vcap;
+  const uint32_t* sc = p.scores + (int64_t)r * p.vcap;   // 512-byte aligned (vcap % 128 == 0)
+  const uint4* sc4 = reinterpret_cast<const uint4*>(sc);
+  const int64_t n4 = (Vs + 3) >> 2;                      // the last vector may pass Vs (< vcap)
+  constexpr int64_t kStep = (int64_t)kTopkThreads * kSweepVec;
+  if (tid == 0) {
+    sh.count = 0;
+    sh.ncand = 0;
+  }
+  __syncthreads();
   pdl_wait();      // the score kernel's keys are complete and visible
 
-  // 1. count keys, per-thread maxima, lower bound L0 (8 loads in flight)
+  // One sweep over the row: appends every key >= thr (thr >= 1; 0 = none)
+  // with its block index to the candidate list, one shared atomic per warp
+  // and step; with `stats`, counts the keys and takes per-thread maxima.
   uint32_t tmax = 0, cnt = 0;
-  for (int64_t base = tid; base < Vs; base += kTopkThreads * kSweepUnroll) {
-    uint32_t x[kSweepUnroll];
+  auto sweep = [&](uint32_t thr, bool stats) {
+    for (int64_t base = 0; base < n4; base += kStep) {
+      uint4 v[kSweepVec];
 #pragma unroll
-    for (int u = 0; u < kSweepUnroll; ++u) {
-      const int64_t i = base + (int64_t)u * kTopkThreads;
-      x[u] = i < Vs ? sc[i] : 0u;
-    }
+      for (int u = 0; u < kSweepVec; ++u) {
+        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
+        v[u] = i < n4 ? ld_cg16(sc4 + i) : make_uint4(0, 0, 0, 0);
+      }
+      uint32_t mask = 0;                                   // bit 4u + j
 #pragma unroll
-    for (int u = 0; u < kSweepUnroll; ++u) {
-      tmax = x[u] > tmax ? x[u] : tmax;
-      cnt += x[u] != 0u;
+      for (int u = 0; u < kSweepVec; ++u) {
+        const int64_t k0 = 4 * (base + (int64_t)u * kTopkThreads + tid);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t x = k0 + j < Vs ? u4_at(v[u], j) : 0u;
+          if (stats) {
+            tmax = x > tmax ? x : tmax;
+            cnt += x != 0u;
+          }
+          mask |= (uint32_t)(thr != 0u && x >= thr) << (4 * u + j);
+        }
+      }
+      if (thr == 0u) continue;
+      int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
+#pragma unroll
+      for (int u = 0; u < kSweepVec; ++u) {
+        const int64_t k0 = 4 * (base + (int64_t)u * kTopkThreads + tid);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (mask >> (4 * u + j) & 1u) {
+            if (slot < kCandCap) {
+              sh.cand_x[slot] = u4_at(v[u], j);
+              sh.cand_i[slot] = (uint32_t)(k0 + j);
+            }
+            ++slot;
+          }
+        }
+      }
     }
-  }
+  };
+
+  // 1. one sweep: the counts and maxima; a row of at most 8192 blocks also
+  // keeps every key as a candidate
+  const uint32_t thr = Vs <= kCandCap ? 1u : 0u;
+  sweep(thr, true);
+  uint32_t nkeys = 0, nonempty = 0, minmax = 0xffffffffu, M = 0;
   {
     uint32_t mn = tmax != 0u ? tmax : 0xffffffffu;
+    uint32_t mx = tmax;
     uint32_t ne = tmax != 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       ne += __shfl_xor_sync(0xffffffffu, ne, o);
       mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    if (lane == 0) { sh.wsum[warp] = cnt; sh.wcnt[warp] = ne; sh.wmin[warp] = mn; }
-    if (tid == 0) sh.count = 0;
+    if (lane == 0) {
+      sh.wsum[warp] = cnt;
+      sh.wcnt[warp] = ne;
+      sh.wmin[warp] = mn;
+      sh.wmax[warp] = mx;
+    }
     __syncthreads();
-  }
-  uint32_t nkeys = 0, nonempty = 0, minmax = 0xffffffffu;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    nkeys += sh.wsum[w];
-    nonempty += sh.wcnt[w];
-    minmax = min(minmax, sh.wmin[w]);
+    for (int w = 0; w < kTopkWarps; ++w) {
+      nkeys += sh.wsum[w];
+      nonempty += sh.wcnt[w];
+      minmax = min(minmax, sh.wmin[w]);
+      M = max(M, sh.wmax[w]);
+    }
   }
   const uint32_t K = nkeys < (uint32_t)kTopkBlocks ? nkeys : (uint32_t)kTopkBlocks;
-  __syncthreads();
+  uint32_t lo = thr;
+  int ncand = sh.ncand;
+  if (K > 0 && thr == 0u) {
+    // 2. a second sweep keeps the keys >= L0, the smallest per-thread
+    // maximum: a lower bound of the K-th largest key when >= K threads hold
+    // a key (K distinct keys -- the maxima -- are >= it); else L0 = 1
+    lo = nonempty >= K ? minmax : 1u;
+    sweep(lo, false);                                      // the first sweep kept none
+    __syncthreads();
+    ncand = sh.ncand;
+  }
+  const bool fits = ncand <= kCandCap;
+  const uint32_t tie_lo = 0x80000000u - (uint32_t)Vs;      // 2^31-1 - (Vs-1)
 
   if (K > 0) {
-    const uint32_t L0 = nonempty >= K ? minmax : 1u;
-    // 2. candidates >= L0 into this warp's region (a register counter per
-    // warp, no atomics; 8 loads in flight)
-    uint32_t wcount = 0;
-    uint32_t* cx = sh.cand_x + warp * kWarpCand;
-    uint32_t* ci = sh.cand_i + warp * kWarpCand;
-    for (int64_t base = 0; base < Vs; base += kTopkThreads * kSweepUnroll) {
-      uint32_t x[kSweepUnroll];
-#pragma unroll
-      for (int u = 0; u < kSweepUnroll; ++u) {
-        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
-        x[u] = i < Vs ? sc[i] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kSweepUnroll; ++u) {
-        const bool take = x[u] != 0u && x[u] >= L0;
-        const unsigned bal = __ballot_sync(0xffffffffu, take);
-        const uint32_t pos = wcount + __popc(bal & ((1u << lane) - 1u));
-        if (take && pos < (uint32_t)kWarpCand) {
-          cx[pos] = x[u];
-          ci[pos] = (uint32_t)(base + (int64_t)u * kTopkThreads + tid);
-        }
-        wcount += __popc(bal);
-      }
-    }
-    if (lane == 0) sh.wcand[warp] = wcount;
-    __syncthreads();
-    bool fits = true;
-    for (int w = 0; w < kTopkWarps; ++w) fits &= sh.wcand[w] <= (uint32_t)kWarpCand;
     if (fits) {
-      // 3. radix select over the candidate regions
-      const Selected sel = radix_select<kCand>(sh, sc, kCandCap, K);
+      // 3. radix select over the candidates
+      const Selected sel = radix_select<false, true>(sh, sh.cand_x, ncand, K, lo, M);
       const uint32_t T = sel.T;
-      const bool all_eq = sel.eq_total == sel.need;
-      // each warp emits from its own region
-      for (uint32_t c = lane; c < ((wcount + 31u) & ~31u); c += 32) {
-        const bool in = c < wcount;
-        const uint32_t x = in ? cx[c] : 0u;
-        emit_warp(sh, in && (x > T || (x == T && all_eq)), x, in ? ci[c] : 0u, lane);
+      for (int base = 0; base < ncand; base += kTopkThreads) {
+        const int c = base + tid;
+        const uint32_t x = c < ncand ? sh.cand_x[c] : 0u;
+        emit_warp(sh, x != 0u && (sel.clean ? x >= T : x > T), x,
+                  c < ncand ? sh.cand_i[c] : 0u, lane);
       }
-      if (!all_eq) {   // surplus ties at T: keep the smallest block indices
-        const Selected si = radix_select<kCandTie>(sh, sc, kCandCap, sel.need, T);
-        for (uint32_t c = lane; c < ((wcount + 31u) & ~31u); c += 32) {
-          const bool in = c < wcount;
-          const bool take = in && cx[c] == T && 0x7fffffffu - ci[c] >= si.T;
-          emit_warp(sh, take, T, in ? ci[c] : 0u, lane);
+      if (!sel.clean) {   // T exact, surplus ties: keep the smallest block indices
+        const Selected si =
+            radix_select<true, true>(sh, sh.cand_x, ncand, sel.need, tie_lo, 0x7fffffffu, T);
+        for (int base = 0; base < ncand; base += kTopkThreads) {
+          const int c = base + tid;
+          const bool take =
+              c < ncand && sh.cand_x[c] == T && 0x7fffffffu - sh.cand_i[c] >= si.T;
+          emit_warp(sh, take, T, c < ncand ? sh.cand_i[c] : 0u, lane);
         }
       }
     } else {
-      // fallback: radix select over all keys of the row (from the workspace)
-      const Selected sel = radix_select<kRow>(sh, sc, Vs, K);
+      // fallback: select over all keys of the row
+      const Selected sel = radix_select<false, false>(sh, sc, Vs, K, 1u, M);
       const uint32_t T = sel.T;
-      const bool all_eq = sel.eq_total == sel.need;
       for (int64_t b0 = 0; b0 < Vs; b0 += kTopkThreads) {
         const int64_t i = b0 + tid;
         const uint32_t x = i < Vs ? sc[i] : 0u;
-        emit_warp(sh, x != 0u && (x > T || (x == T && all_eq)), x, i, lane);
+        emit_warp(sh, x != 0u && (sel.clean ? x >= T : x > T), x, i, lane);
       }
-      if (!all_eq) {
-        const Selected si = radix_select<kRowTie>(sh, sc, Vs, sel.need, T);
+      if (!sel.clean) {
+        const Selected si =
+            radix_select<true, false>(sh, sc, Vs, sel.need, tie_lo, 0x7fffffffu, T);
         for (int64_t b0 = 0; b0 < Vs; b0 += kTopkThreads) {
           const int64_t i = b0 + tid;
           const bool take = i < Vs && sc[i] == T && 0x7fffffffu - (uint32_t)i >= si.T;
@@ -836,47 +923,44 @@ topk_kernel(const SelectParams p) {
     __syncthreads();
   }
 
-  // 4. order: each warp sorts its 32 keys descending with shuffles; a key's
-  // final position is its place in its warp's list plus, for every other
-  // warp's list, how many keys there are larger (binary search).  Kept keys
-  // are distinct and nonzero, so their positions are exactly 0..K-1.
+  // 4. order: a bitonic sort of the 512 slots (kept pairs, then zeros),
+  // descending; partners closer than a warp exchange by shuffles, the others
+  // through shared memory (two buffers, one barrier per step).  Kept keys
+  // are distinct and nonzero, so slot i ends with the i-th largest.
   unsigned long long a = tid < (int)K ? sh.keys[tid] : 0ull;
+  {
+    unsigned long long* const buf0 = sh.keys;
+    unsigned long long* const buf1 = reinterpret_cast<unsigned long long*>(sh.cand_x);
+    int nb = 0;
+    __syncthreads();                     // every read of keys[] above is done
 #pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
+    for (int k = 2; k <= kTopkThreads; k <<= 1) {
 #pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const unsigned long long b = shfl_xor_u64(a, j);
-      const bool desc = (lane & k) == 0 || k == 32;
-      const bool lower = (lane & j) == 0;
-      const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
-      a = (desc == lower) ? hi : lo;
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        unsigned long long b;
+        if (j >= 32) {
+          unsigned long long* const bf = nb ? buf1 : buf0;
+          bf[tid] = a;
+          __syncthreads();
+          b = bf[tid ^ j];
+          nb ^= 1;
+        } else {
+          b = shfl_xor_u64(a, j);
+        }
+        const bool desc = (tid & k) == 0;
+        const bool lower = (tid & j) == 0;
+        const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+        a = (desc == lower) ? hi : lo;
+      }
     }
   }
-  __syncthreads();
-  sh.keys[tid] = a;
-  __syncthreads();
-  if (a != 0ull) {
-    int rank = lane;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      if (w == warp) continue;
-      const unsigned long long* lst = sh.keys + w * 32;
-      int pos = 0;                                   // keys in lst larger than a
-      if (lst[31] > a) {
-        pos = 32;
-      } else {
-#pragma unroll
-        for (int step = 16; step > 0; step >>= 1)
-          if (lst[pos + step - 1] > a) pos += step;
-      }
-      rank += pos;
-    }
-    // expand the kept block at its position
+  if (tid < (int)K) {   // expand the kept block at its position
     const int32_t b = (int32_t)(0xffffffffu - (uint32_t)(a & 0xffffffffull));
     const int32_t tok = b * kRatio;
-    out[4 * rank + 0] = tok;
-    out[4 * rank + 1] = tok + 1;
-    out[4 * rank + 2] = tok + 2;
-    out[4 * rank + 3] = tok + 3;
+    out[4 * tid + 0] = tok;
+    out[4 * tid + 1] = tok + 1;
+    out[4 * tid + 2] = tok + 2;
+    out[4 * tid + 3] = tok + 3;
   }
   // then the tail, then -1
   const int64_t tail0 = rs.V * kRatio;

@@ -89,6 +89,25 @@ def test_select_exact_ties_and_duplicate_pages():
     _check(w)
 
 
+@pytest.mark.parametrize("distinct", [2, 4])
+def test_select_long_rows_heavy_ties(distinct):
+    # rows longer than the top-k's 8192-key candidate list: with 2 distinct
+    # keys about half of a 32768-block row ties at the largest score (the
+    # candidates overflow: select over the whole row); with 4, a quarter
+    # (the lower-bound sweep, then the tie rule over the candidates)
+    w = W.build("longties", [131072, 40003, 65539], distinct_keys=distinct, seed=13 + distinct,
+                device=DEV)
+    _check(w)
+
+
+def test_select_all_zero_scores_long_row():
+    # every key equals bits(+0)+1: 32768 ties, kept in block order
+    w = W.build("zeros_long", [131072], seed=14, device=DEV)
+    w.q_sel.zero_()
+    got, _, _ = _check(w)
+    assert got[0, :2048].tolist() == list(range(2048))
+
+
 def test_select_all_zero_scores():
     w = W.build("zeros", [9215, 2051], seed=4, device=DEV)
     w.q_sel.zero_()
