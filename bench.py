@@ -391,6 +391,10 @@ def run_ours(args, world, rank, local):
         raise SystemExit(f"bench.py: device error word {int(err.item())}")
 
     peak, peak_kind = _peaks()
+    fused = None
+    if not args.no_fused:
+        fused = fused_variant(args, w, R, world, dev, stream, idx, out, err, peak,
+                              sel_bytes + att_bytes)
     fp8 = None
     if not args.no_fp8:
         fp8 = fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak)
@@ -439,6 +443,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms, "steps": Ke},
+        "fused_select_attend": fused,
         "fp8_compressed_cache": fp8,
         "metadata_builder": meta,
         "speculative_decode": spec,
@@ -448,6 +453,43 @@ def run_ours(args, world, rank, local):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def fused_variant(args, w, R, world, dev, stream, idx, out, err, peak, step_bytes):
+    """One decode step through qsa_select_attend (score kernel + follower
+    kernel that takes each row's top-k and attention as soon as the row is
+    scored), on the same workload and outputs."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    ws = torch.empty(qsa.qsa_select_attend_workspace_bytes(R, w.cmp_page_table.shape[1]),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                              w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                              w.kv_page_table, indices=idx, out=out, workspace=ws,
+                              error_word=err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(1, min(args.steps, 500))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    if int(err.item()) != 0:
+        raise SystemExit(f"bench.py: device error word {int(err.item())} (fused path)")
+    ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    return {"value": R * world / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms, "steps": K,
+            "step_hbm_gbs": gbs, "step_frac_of_peak": gbs / peak,
+            "launches_per_step": 2, "memsets_per_step": 1}
 
 
 def fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak):
@@ -680,6 +722,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8-E4M3 compressed-cache measurement")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the one-call select+attend (qsa_select_attend) measurement")
     ap.add_argument("--no-spec", action="store_true",
                     help="skip the speculative-decode (4 tokens per request) measurement")
     ap.add_argument("--no-indexer", action="store_true",

@@ -9,6 +9,8 @@
  *                             "Exact contracts" / Selection.
  *   qsa_sparse_attention      same page, Summary (exact-packed attention
  *                             bullet) and "Exact contracts" / Attention.
+ *   qsa_select_attend         both in one call, the attention of early rows
+ *                             overlapping the scoring of later ones.
  *
  * The visible-block rule used by selection comes from qsa_cache.py
  * (_build_qsa_metadata_kernel: visible = max(0, min((pos+1)//4, seq_len//4))).
@@ -201,6 +203,63 @@ QSA_API qsa_status qsa_sparse_attention(
     const void* indices, qsa_dtype idx_dtype, int64_t index_width, int64_t idx_stride0,
     float scale,
     void* out, qsa_dtype out_dtype, const int64_t out_strides[3],
+    void* workspace, size_t workspace_bytes,
+    uint32_t* error_word, qsa_stream_t stream);
+
+/*
+ * Workspace for qsa_select_attend: bytes needed for num_rows rows whose
+ * compressed page table has cmp_pt_cols columns.  Alignment 256 bytes.
+ */
+QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols);
+
+/*
+ * qsa_select_attend -- one decode step: qsa_select_paged_tokens followed by
+ * qsa_sparse_attention over the indices it selects ("vLLM: integrate FP16
+ * packed QSA extension", Summary: the fused selection and the exact-packed
+ * attention kernel; "Exact contracts" / Selection and Attention), with the
+ * attention of early rows running while later rows are still being scored.
+ *
+ * Results: out_indices is bit-identical to qsa_select_paged_tokens on the
+ * same inputs; out is the attention of qsa_sparse_attention over those
+ * indices (FP32 accumulation; the index list is split into runs of 512
+ * entries instead of 256, so the last bits of out may differ from the
+ * two-call path, within the same bound against the exact result).
+ *
+ * Arguments: the selection's, as qsa_select_paged_tokens (num_reqs rows in
+ * both page tables), then the attention's, as qsa_sparse_attention without
+ * its own token_to_request and index list (it uses token_to_request and
+ * out_indices); one workspace of >= qsa_select_attend_workspace_bytes(
+ * num_rows, cmp_pt_cols) bytes, 256-byte aligned.  out_indices and out must
+ * not overlap each other, any input or the workspace.
+ *
+ * How it runs: a memset of the workspace's counters, then two kernels on
+ * the stream: the score kernel on most SMs, and a follower kernel
+ * (launched as its programmatic dependent) on the others, which takes each
+ * row's top-k once the row's keys are scored and then the row's attention.
+ * The follower waits on counters the score kernel publishes; every wait
+ * gives up after 1 s (QSA_DERR_TIMEOUT in *error_word; the outputs are then
+ * incomplete), so a fault can never hang the GPU.  Calls that share a
+ * workspace must not overlap on the GPU.
+ */
+QSA_API qsa_status qsa_select_attend(
+    const void* q_sel, qsa_dtype q_sel_dtype, int64_t num_rows,
+    const int64_t q_sel_strides[3],
+    const void* cmp_cache, qsa_dtype cmp_dtype, const int64_t cmp_shape[4],
+    const int64_t cmp_strides[4],
+    const void* cmp_page_table, qsa_dtype cmp_pt_dtype, int64_t num_reqs,
+    int64_t cmp_pt_cols, int64_t cmp_pt_stride0,
+    const void* token_to_request, qsa_dtype t2r_dtype,
+    const void* seq_lens, qsa_dtype seq_lens_dtype,
+    const void* query_positions, qsa_dtype qpos_dtype,
+    int32_t token_topk, int32_t compress_ratio,
+    void* out_indices, qsa_dtype out_dtype, int64_t out_width, int64_t out_stride0,
+    const void* q_attn, qsa_dtype q_attn_dtype, const int64_t q_attn_strides[3],
+    const void* k_cache, const void* v_cache, qsa_dtype kv_dtype,
+    const int64_t kv_shape[4], const int64_t k_strides[4], const int64_t v_strides[4],
+    const void* kv_page_table, qsa_dtype kv_pt_dtype,
+    int64_t kv_pt_cols, int64_t kv_pt_stride0,
+    float scale,
+    void* out, qsa_dtype out_attn_dtype, const int64_t out_strides[3],
     void* workspace, size_t workspace_bytes,
     uint32_t* error_word, qsa_stream_t stream);
 

@@ -38,7 +38,8 @@ STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE"
 
 EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
-            "qsa_sparse_attention", "qsa_static_scratch_bytes",
+            "qsa_sparse_attention", "qsa_select_attend_workspace_bytes", "qsa_select_attend",
+            "qsa_static_scratch_bytes",
             "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata",
             "qsa_paged_mqa_logits", "qsa_top_k_per_row_decode")
 
@@ -91,6 +92,22 @@ def load_library(path: str | None = None):
             vp, vp, ctypes.c_int, p64, p64, p64,
             vp, ctypes.c_int, i64, i64, i64,
             vp, ctypes.c_int,
+            vp, ctypes.c_int, i64, i64,
+            ctypes.c_float,
+            vp, ctypes.c_int, p64,
+            vp, sz, vp, vp]
+        lib.qsa_select_attend_workspace_bytes.restype = sz
+        lib.qsa_select_attend_workspace_bytes.argtypes = [i64, i64]
+        lib.qsa_select_attend.restype = ctypes.c_int
+        lib.qsa_select_attend.argtypes = [
+            vp, ctypes.c_int, i64, p64,
+            vp, ctypes.c_int, p64, p64,
+            vp, ctypes.c_int, i64, i64, i64,
+            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+            i32, i32,
+            vp, ctypes.c_int, i64, i64,
+            vp, ctypes.c_int, p64,
+            vp, vp, ctypes.c_int, p64, p64, p64,
             vp, ctypes.c_int, i64, i64,
             ctypes.c_float,
             vp, ctypes.c_int, p64,
@@ -244,6 +261,63 @@ def qsa_decode(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens, que
     out = qsa_sparse_attention(q_attn, k_cache, v_cache, kv_page_table, token_to_request,
                                indices, scale=scale, out=out, workspace=att_workspace,
                                error_word=error_word, stream=stream)
+    return indices, out
+
+
+def qsa_select_attend_workspace_bytes(num_rows: int, cmp_pt_cols: int) -> int:
+    return int(load_library().qsa_select_attend_workspace_bytes(num_rows, cmp_pt_cols))
+
+
+def qsa_select_attend(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
+                      query_positions, q_attn, k_cache, v_cache, kv_page_table,
+                      scale: float = 1.0 / 16.0, indices=None, out=None, workspace=None,
+                      error_word=None, stream=None):
+    """One decode step in one call (include/qsa.h, qsa_select_attend): the
+    selection's indices [R,2051] int32 and the attention output [R,3,256]
+    FP16, with the attention of early rows overlapping the scoring of later
+    ones.  Both page tables are indexed by token_to_request."""
+    lib = load_library()
+    if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
+        raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
+    if q_attn.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or kv_page_table.dim() != 2:
+        raise QSAError(3, "q_attn [R,3,256], k/v [P,512,1,256], K/V page table 2-D expected")
+    if k_cache.shape != v_cache.shape:
+        raise QSAError(3, "k_cache and v_cache shapes differ")
+    if kv_page_table.shape[0] != cmp_page_table.shape[0]:
+        raise QSAError(3, "both page tables need one row per request")
+    for t in (cmp_page_table, kv_page_table):
+        if t.stride(1) != 1 and t.shape[1] > 1:
+            raise QSAError(4, "page table columns must be contiguous")
+    R = q_sel.shape[0]
+    if indices is None:
+        indices = torch.empty((R, OUT_WIDTH), dtype=torch.int32, device=q_sel.device)
+    if indices.dim() != 2 or (indices.stride(1) != 1 and indices.shape[1] > 1):
+        raise QSAError(4, "indices must be [R,2051] with contiguous columns")
+    if out is None:
+        out = torch.empty((R, 3, 256), dtype=torch.float16, device=q_sel.device)
+    cols = cmp_page_table.shape[1]
+    need = qsa_select_attend_workspace_bytes(R, cols)
+    if workspace is None:
+        workspace = _workspace(need, q_sel.device)
+    st = lib.qsa_select_attend(
+        _ptr(q_sel), _tag(q_sel), R, _arr(q_sel.stride()),
+        _ptr(cmp_cache), _tag(cmp_cache), _arr(cmp_cache.shape), _arr(cmp_cache.stride()),
+        _ptr(cmp_page_table), _tag(cmp_page_table), cmp_page_table.shape[0], cols,
+        cmp_page_table.stride(0),
+        _ptr(token_to_request), _tag(token_to_request), _ptr(seq_lens), _tag(seq_lens),
+        _ptr(query_positions), _tag(query_positions),
+        TOKEN_TOPK, COMPRESS_RATIO,
+        _ptr(indices), _tag(indices), indices.shape[1], indices.stride(0),
+        _ptr(q_attn), _tag(q_attn), _arr(q_attn.stride()),
+        _ptr(k_cache), _ptr(v_cache), _tag(k_cache) if k_cache.dtype == v_cache.dtype else 0,
+        _arr(k_cache.shape), _arr(k_cache.stride()), _arr(v_cache.stride()),
+        _ptr(kv_page_table), _tag(kv_page_table), kv_page_table.shape[1],
+        kv_page_table.stride(0),
+        float(scale),
+        _ptr(out), _tag(out), _arr(out.stride()),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(error_word), _stream(stream))
+    _check(st)
     return indices, out
 
 

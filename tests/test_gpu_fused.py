@@ -1,0 +1,167 @@
+"""GPU parity for qsa_select_attend, the one-call decode step: the selection's
+indices must be bit-identical to the oracle's (and to qsa_select_paged_tokens),
+and the attention output within 2e-3 of the binary64 oracle over those
+indices ("vLLM: integrate FP16 packed QSA extension", Summary and "Exact
+contracts"/Selection and Attention; the pages' tie, tail, saturation and
+multi-request cases).
+
+The fused path overlaps the attention of early rows with the scoring of
+later ones (a score kernel and a follower kernel that waits on per-row
+counters), so these tests also cover its row chunks (more than 1024 rows),
+speculative rows that share a request, bad ids, and repeated calls on a
+dirty workspace.  Tolerance as in test_gpu_attention.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparse_paged_attention_qsa_gb300 as qsa
+from sparse_paged_attention_qsa_gb300 import workloads as W
+from tests._util import oracle_attention, oracle_select
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 2e-3
+
+
+def _fused(w, pt=None, t2r=None, workspace=None):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx, out = qsa.qsa_select_attend(
+        w.q_sel, w.cmp_cache, w.cmp_page_table if pt is None else pt,
+        w.token_to_request if t2r is None else t2r, w.seq_lens, w.query_positions,
+        w.q_attn, w.k_view, w.v_view, w.kv_page_table, workspace=workspace, error_word=err)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), out.float().cpu().numpy(), int(err.item())
+
+
+def _check(w, rows=None, pt=None, t2r=None):
+    got_idx, got_out, gerr = _fused(w, pt=pt, t2r=t2r)
+    rows = list(range(w.R)) if rows is None else list(rows)
+    exp_idx, oerr = oracle_select(w, rows=rows, cmp_page_table=pt, token_to_request=t2r)
+    for i, r in enumerate(rows):
+        if not np.array_equal(got_idx[r], exp_idx[i]):
+            bad = np.nonzero(got_idx[r] != exp_idx[i])[0]
+            raise AssertionError(f"row {r}: {len(bad)} index mismatches, first at {bad[0]}")
+    full = np.full((w.R, 2051), -1, np.int32)
+    full[rows] = exp_idx                    # the oracle's own index lists
+    exp_out, _ = oracle_attention(w, full, rows=rows, token_to_request=t2r)
+    diff = np.abs(got_out[rows] - exp_out).max() if rows else 0.0
+    assert diff <= TOL, f"max abs error {diff}"
+    return got_idx, got_out, gerr, oerr
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_fused_configs(cfg):
+    w = W.config(cfg, device=DEV)
+    _, _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
+def test_fused_config4_full_size_sampled_rows():
+    w = W.config(4, device=DEV)
+    got_idx, got_out, gerr, _ = _check(w, rows=[0, 1, 77, 128, 200, 255])
+    assert gerr == 0
+    assert (got_idx[:, :2048] >= 0).all() and (got_idx[:, 2048:] == -1).all()
+    assert np.isfinite(got_out).all()
+
+
+def test_fused_matches_two_call_path():
+    w = W.config(2, device=DEV)
+    idx2, out2 = qsa.qsa_decode(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                                w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                                w.kv_page_table)
+    got_idx, got_out, gerr = _fused(w)
+    assert gerr == 0
+    assert np.array_equal(got_idx, idx2.cpu().numpy())
+    assert np.abs(got_out - out2.float().cpu().numpy()).max() <= TOL
+
+
+@pytest.mark.parametrize("lens", [[0, 1, 3, 4, 7, 515, 516, 519, 1027], [2051, 2053, 9215, 131072]])
+def test_fused_short_empty_and_saturated_rows(lens):
+    w = W.build("edge", lens, seed=sum(lens) % 1000 + 3, device=DEV)
+    _, got_out, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+    assert (got_out[0] == 0).all() if lens[0] == 0 else True   # no valid entry -> zeros
+
+
+def test_fused_heavy_ties_and_duplicate_pages():
+    w = W.build("ties", [6003, 4099, 30001, 515, 131072], distinct_keys=2, dup_mapping=True,
+                seed=31, device=DEV)
+    _check(w)
+
+
+def test_fused_speculative_rows_share_pages():
+    # 12 requests x 4 query tokens: rows of one request are scored from one
+    # pass over its pages; each row still gets its own visible blocks
+    from oracle import metadata as M
+    rng = np.random.default_rng(90)
+    L = [int(x) for x in rng.integers(600, 40000, size=12)]
+    L[0], L[1] = 2051, 2052
+    w = W.build("spec4", L, query_lens=[4] * 12, seed=91, device=DEV)
+    m = M.build_metadata(w.query_start_loc.cpu().numpy(), w.seq_lens.cpu().numpy(),
+                         w.cmp_page_table.cpu().numpy(), w.R, storage_block_size=128,
+                         compress_ratio=4, common_slot_mapping=np.zeros(w.R, np.int64))
+    w = W.Workload(**{**w.__dict__,
+                      "token_to_request": torch.from_numpy(m["token_to_req"]).to(DEV),
+                      "query_positions": torch.from_numpy(m["logical_positions"]).to(DEV)})
+    _, _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
+def test_fused_bad_ids_set_error_bits():
+    w = W.build("bad", [3000, 3000, 3000, 9000], seed=36, device=DEV)
+    pt = w.cmp_page_table.clone()
+    pt[1, 2] = w.cmp_cache.shape[0] + 5         # compressed page beyond the pool
+    pt[3, 0] = -1                               # unmapped compressed page
+    t2r = torch.tensor([0, 1, 9, 3], dtype=torch.int32, device=DEV)   # row 2: no request
+    got_idx, got_out, gerr, oerr = _check(w, pt=pt, t2r=t2r)
+    assert gerr == oerr == (qsa.DERR_REQUEST | qsa.DERR_CMP_PAGE)
+    assert (got_idx[2] == -1).all() and (got_out[2] == 0).all()
+
+
+def test_fused_fp8_keys():
+    w = W.config(2, device=DEV, cmp_dtype="fp8")
+    _, _, gerr, oerr = _check(w, rows=list(range(0, 64, 7)))
+    assert gerr == oerr == 0
+
+
+def test_fused_more_rows_than_one_launch():
+    # 1100 rows run as a 1024-row launch and a 76-row launch on the stream
+    rng = np.random.default_rng(92)
+    L = [int(x) for x in rng.integers(300, 3000, size=1100)]
+    w = W.build("many", L, seed=93, device=DEV)
+    _, _, gerr, oerr = _check(w, rows=[0, 1, 511, 1023, 1024, 1025, 1099])
+    assert gerr == 0
+
+
+def test_fused_repeat_calls_on_dirty_workspace():
+    w = W.config(1, device=DEV)
+    a_idx, a_out, _ = _fused(w)
+    need = qsa.qsa_select_attend_workspace_bytes(w.R, w.cmp_page_table.shape[1])
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)   # counters start dirty
+    for _ in range(3):
+        b_idx, b_out, gerr = _fused(w, workspace=ws)
+        assert gerr == 0
+        assert np.array_equal(a_idx, b_idx) and np.array_equal(a_out, b_out)
+
+
+def test_fused_fails_closed():
+    w = W.config(0, device=DEV)
+    with pytest.raises(qsa.QSAError) as e:      # attention query dtype
+        qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                              w.seq_lens, w.query_positions, w.q_attn.float(), w.k_view,
+                              w.v_view, w.kv_page_table)
+    assert e.value.status == 2
+    with pytest.raises(qsa.QSAError) as e:      # workspace too small
+        qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                              w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                              w.kv_page_table,
+                              workspace=torch.empty(256, dtype=torch.uint8, device=DEV))
+    assert e.value.status == 7
+    idx = torch.empty((1, 2051), dtype=torch.int32, device=DEV)
+    with pytest.raises(qsa.QSAError) as e:      # attention output aliases the indices
+        qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                              w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                              w.kv_page_table, indices=idx,
+                              out=idx.view(torch.float16).as_strided((1, 3, 256), (768, 256, 1)))
+    assert e.value.status == 8
