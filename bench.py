@@ -413,7 +413,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         threads = max(1, min(os.cpu_count() or 1, 16))
         sample = OracleSample(w, range(min(threads, R)))
-        n = 2 * len(sample.rows)
+        rate0, _ = oracle_rate(sample, 2 * len(sample.rows), threads)   # calibration
+        n = max(2 * len(sample.rows), int(rate0 * 10.0))                 # about 10 s of rows
         rate, dt = oracle_rate(sample, n, threads)
         cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} decode rows (select+attend) over {len(sample.rows)} rows of "

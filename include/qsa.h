@@ -288,7 +288,7 @@ QSA_API qsa_status qsa_select_attend(
  * Arguments, validation and results are those of qsa_select_paged_tokens
  * without the workspace pair.
  */
-#define QSA_STATIC_SCRATCH_BYTES (4u << 20)  /* 4 MiB: 1,048,576 score slots */
+#define QSA_STATIC_SCRATCH_BYTES (4u << 20)  /* 4 MiB: keys of 986,895 blocks */
 
 QSA_API size_t qsa_static_scratch_bytes(void);
 

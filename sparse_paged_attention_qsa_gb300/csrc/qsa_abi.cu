@@ -280,6 +280,7 @@ qsa_status qsa_select_paged_tokens(
       if (overlaps(e, s)) return QSA_ERR_ALIAS;
   }
   p.scores = static_cast<uint32_t*>(workspace);
+  p.umax = p.scores + num_rows * p.vcap;
   const cudaError_t e = qsa::launch_select(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
@@ -378,6 +379,7 @@ qsa_status qsa_select_attend(
   }
   unsigned char* w = static_cast<unsigned char*>(workspace);
   p.scores = reinterpret_cast<uint32_t*>(w);
+  p.umax = p.scores + num_rows * p.vcap;
   p.sync = reinterpret_cast<uint32_t*>(w + l.sync);
   a.part = reinterpret_cast<float*>(w + l.part);
   a.nsplit = qsa::kFusedSplits;

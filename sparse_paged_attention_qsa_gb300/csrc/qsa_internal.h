@@ -45,6 +45,7 @@ struct SelectParams {
   int32_t* out;               // [R, 2051], row stride out_stride0
   int64_t out_stride0;
   uint32_t* scores;           // workspace: [R, vcap] ordered score keys
+  uint32_t* umax;             // workspace: [R, vcap/16] largest key of each run of 16 blocks
   int64_t vcap;               // pt_cols * 128
   uint32_t* err;              // nullable
   uint32_t* sync;             // fused select -> attend only: counters (kSync*), else null

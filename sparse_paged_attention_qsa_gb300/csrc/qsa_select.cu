@@ -56,6 +56,9 @@ static_assert(2 * kScoreWarps == kKeyGroups, "each consumer warp takes whole key
 constexpr int kMaxRows = 1024;                          // rows per launch (row tables in smem)
 static_assert(kMaxRows == kFusedMaxRows, "one row chunk per fused launch");
 constexpr int kChunkPages = 32;  // fused path: pages of a group per unit (1 MiB of fp16 keys)
+// The score kernel also keeps the largest key of each run of 16 blocks (one
+// warp step: two groups of 8 keys), so the top-k reads 1/16 of a row first.
+constexpr int kUnitKeys = 16;
 constexpr int kGroupRows = 8;    // rows of one request scored from one page pass (aligned windows)
 // row tables: req, visible blocks; group tables: first row (+ sentinel), pages,
 // weighted page prefix (64-bit, + total)
@@ -178,20 +181,21 @@ __device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float 
   return d;
 }
 
-// Two E4M3 values (low byte = even dim) -> fp16 pair, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t v) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
-      : "=r"(d) : "r"(v));
-  return d;
+// Four E4M3 values (one 32-bit word, byte 0 = lowest dim) -> two fp16 pairs,
+// exact: each 16-bit half of the word is one cvt (no masks or shifts).
+__device__ __forceinline__ void e4m3x4_to_h(uint32_t v, uint32_t& a, uint32_t& b) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(a), "=r"(b)
+      : "r"(v));
 }
 
 // 16 E4M3 values (one 16-byte chunk) -> 16 fp16 values as two 16-byte words.
 __device__ __forceinline__ void e4m3x16_to_h(uint4 c, uint4& lo, uint4& hi) {
-  lo = make_uint4(e4m3x2_to_h2(c.x & 0xffffu), e4m3x2_to_h2(c.x >> 16),
-                  e4m3x2_to_h2(c.y & 0xffffu), e4m3x2_to_h2(c.y >> 16));
-  hi = make_uint4(e4m3x2_to_h2(c.z & 0xffffu), e4m3x2_to_h2(c.z >> 16),
-                  e4m3x2_to_h2(c.w & 0xffffu), e4m3x2_to_h2(c.w >> 16));
+  e4m3x4_to_h(c.x, lo.x, lo.y);
+  e4m3x4_to_h(c.y, lo.z, lo.w);
+  e4m3x4_to_h(c.z, hi.x, hi.y);
+  e4m3x4_to_h(c.w, hi.z, hi.w);
 }
 
 // Score of one key held as four 32-dim slices by a quad of lanes, reduced in
@@ -554,6 +558,9 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
             const int nk = min(row_vs[row0 + j] - col * kCmpPageKeys, kCmpPageKeys);
             uint32_t* zr = p.scores + (int64_t)(row0 + j) * p.vcap + col * kCmpPageKeys;
             for (int k = 0; k < nk; ++k) zr[k] = 0u;
+            uint32_t* zu = p.umax + (int64_t)(row0 + j) * (p.vcap / kUnitKeys) +
+                           col * (kCmpPageKeys / kUnitKeys);
+            for (int k = 0; kUnitKeys * k < nk; ++k) zu[k] = 0u;
           }
           report(p.err, kErrCmpPage);
         }
@@ -632,6 +639,8 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
             const int nk = min(row_vs[row0 + j] - b0, kCmpPageKeys);
             uint32_t* zr = p.scores + (int64_t)(row0 + j) * p.vcap + b0;
             for (int k = 0; k < nk; ++k) zr[k] = 0u;
+            uint32_t* zu = p.umax + (int64_t)(row0 + j) * (p.vcap / kUnitKeys) + b0 / kUnitKeys;
+            for (int k = 0; kUnitKeys * k < nk; ++k) zu[k] = 0u;
           }
           report(p.err, kErrCmpPage);
           pg = -1;
@@ -655,6 +664,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
     uint32_t q[kSelHeads][16];
     int loaded_row = -1;
     uint32_t* srow = nullptr;
+    uint32_t* urow = nullptr;
     for (int64_t used = 0;; ++used) {
       const int s = (int)(used % kStages);
       const uint32_t ph = (uint32_t)((used / kStages) & 1);
@@ -679,14 +689,21 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
         if (row != loaded_row) {
           loaded_row = row;
           srow = p.scores + (int64_t)row * p.vcap;
+          urow = p.umax + (int64_t)row * (p.vcap / kUnitKeys);
           load_query_slice(p.q_sel + (int64_t)row * kSelHeads * kSelDim, t, q);
         }
+        uint32_t um = 0;                     // the unit's (these 16 keys') largest key
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint32_t key = quad_score(q, kv[g], t);
           const int k = (g0 + g) * 8 + kslot;
-          if (t == 0 && k < nk) srow[d.b0 + k] = key;
+          if (k < nk) {
+            if (t == 0) srow[d.b0 + k] = key;
+            um = key > um ? key : um;
+          }
         }
+        um = __reduce_max_sync(0xffffffffu, um);
+        if (lane == 0) urow[(d.b0 + 8 * g0) / kUnitKeys] = um;   // 8 * g0 < nk here
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
@@ -731,23 +748,23 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 8192;                          // candidate (key, block) pairs
-constexpr int kSweepVec = 8;                            // 16-byte loads in flight per thread
+constexpr int kUnitCap = 4096;                          // unit maxima staged in smem
 constexpr int kDigitBits = 12;
 constexpr int kBins = 1 << kDigitBits;                  // 4096 histogram bins
 constexpr int kBinsPerThread = kBins / kTopkThreads;    // 8
 
 struct TopkShared {
-  uint32_t hist[kBins];
+  uint32_t hist[kBins];            // radix histogram; between selects, the hit-unit list
+  uint32_t umax[kUnitCap];         // the row's unit maxima (rows of <= 65536 blocks)
   unsigned long long keys[kTopkBlocks];
   uint32_t cand_x[kCandCap];
   uint32_t cand_i[kCandCap];
   uint32_t wsum[kTopkWarps];
-  uint32_t wcnt[kTopkWarps];
   uint32_t wmin[kTopkWarps];
   uint32_t wmax[kTopkWarps];
   uint32_t found_digit, found_above;
   int count;                       // kept pairs in keys[]
-  int ncand;
+  int nhit, ncand;
 };
 constexpr size_t kTopkSmem = sizeof(TopkShared);
 
@@ -917,104 +934,125 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
   if (tid == 0 && rs.V > p.vcap) report(p.err, kErrCmpPage);
   const int64_t Vs = rs.V < p.vcap ? rs.V : p.vcap;
   const uint32_t* sc = p.scores + (int64_t)r * p.vcap;   // 512-byte aligned (vcap % 128 == 0)
-  const uint4* sc4 = reinterpret_cast<const uint4*>(sc);
-  const int64_t n4 = (Vs + 3) >> 2;                      // the last vector may pass Vs (< vcap)
-  constexpr int64_t kStep = (int64_t)kTopkThreads * kSweepVec;
+  const int64_t nu = (Vs + kUnitKeys - 1) / kUnitKeys;   // units of 16 blocks
+  const uint32_t* ur = p.umax + (int64_t)r * (p.vcap / kUnitKeys);   // 32-byte aligned rows
+  const bool u_in_smem = nu <= kUnitCap;
+  const uint32_t* usrc = u_in_smem ? sh.umax : ur;
   if (tid == 0) {
     sh.count = 0;
+    sh.nhit = 0;
     sh.ncand = 0;
   }
   __syncthreads();
   if (kStandalone) pdl_wait();      // the score kernel's keys are complete and visible
 
-  // One sweep over the row: appends every key >= thr (thr >= 1; 0 = none)
-  // with its block index to the candidate list, one shared atomic per warp
-  // and step; with `stats`, counts the keys and takes per-thread maxima.
-  uint32_t tmax = 0, cnt = 0;
-  auto sweep = [&](uint32_t thr, bool stats) {
-    for (int64_t base = 0; base < n4; base += kStep) {
-      uint4 v[kSweepVec];
+  // 1. unit maxima: how many are nonzero, the smallest nonzero, the largest
+  // (M, the row's largest key); staged in shared memory
+  uint32_t nz = 0, umin = 0xffffffffu, M = 0;
+  {
+    const uint4* u4 = reinterpret_cast<const uint4*>(ur);
+    const int64_t nu4 = (nu + 3) >> 2;                   // the last vector may pass nu
+    for (int64_t b = tid; b < nu4; b += 2 * kTopkThreads) {
+      uint4 v[2];
 #pragma unroll
-      for (int u = 0; u < kSweepVec; ++u) {
-        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
-        v[u] = i < n4 ? ld_cg16(sc4 + i) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 2; ++u) {
+        const int64_t i = b + (int64_t)u * kTopkThreads;
+        v[u] = i < nu4 ? ld_cg16(u4 + i) : make_uint4(0, 0, 0, 0);
       }
-      uint32_t mask = 0;                                   // bit 4u + j
 #pragma unroll
-      for (int u = 0; u < kSweepVec; ++u) {
-        const int64_t k0 = 4 * (base + (int64_t)u * kTopkThreads + tid);
+      for (int u = 0; u < 2; ++u) {
+        const int64_t g0 = 4 * (b + (int64_t)u * kTopkThreads);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t x = k0 + j < Vs ? u4_at(v[u], j) : 0u;
-          if (stats) {
-            tmax = x > tmax ? x : tmax;
-            cnt += x != 0u;
-          }
-          mask |= (uint32_t)(thr != 0u && x >= thr) << (4 * u + j);
-        }
-      }
-      if (thr == 0u) continue;
-      int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
-#pragma unroll
-      for (int u = 0; u < kSweepVec; ++u) {
-        const int64_t k0 = 4 * (base + (int64_t)u * kTopkThreads + tid);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (mask >> (4 * u + j) & 1u) {
-            if (slot < kCandCap) {
-              sh.cand_x[slot] = u4_at(v[u], j);
-              sh.cand_i[slot] = (uint32_t)(k0 + j);
-            }
-            ++slot;
-          }
+          const uint32_t x = g0 + j < nu ? u4_at(v[u], j) : 0u;
+          if (u_in_smem && g0 + j < nu) sh.umax[g0 + j] = x;
+          nz += x != 0u;
+          umin = x != 0u && x < umin ? x : umin;
+          M = x > M ? x : M;
         }
       }
     }
-  };
-
-  // 1. one sweep: the counts and maxima; a row of at most 8192 blocks also
-  // keeps every key as a candidate
-  const uint32_t thr = Vs <= kCandCap ? 1u : 0u;
-  sweep(thr, true);
-  uint32_t nkeys = 0, nonempty = 0, minmax = 0xffffffffu, M = 0;
-  {
-    uint32_t mn = tmax != 0u ? tmax : 0xffffffffu;
-    uint32_t mx = tmax;
-    uint32_t ne = tmax != 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      ne += __shfl_xor_sync(0xffffffffu, ne, o);
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      nz += __shfl_xor_sync(0xffffffffu, nz, o);
+      umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, o));
+      M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
     }
     if (lane == 0) {
-      sh.wsum[warp] = cnt;
-      sh.wcnt[warp] = ne;
-      sh.wmin[warp] = mn;
-      sh.wmax[warp] = mx;
+      sh.wsum[warp] = nz;
+      sh.wmin[warp] = umin;
+      sh.wmax[warp] = M;
     }
     __syncthreads();
+    nz = 0;
     for (int w = 0; w < kTopkWarps; ++w) {
-      nkeys += sh.wsum[w];
-      nonempty += sh.wcnt[w];
-      minmax = min(minmax, sh.wmin[w]);
+      nz += sh.wsum[w];
+      umin = min(umin, sh.wmin[w]);
       M = max(M, sh.wmax[w]);
     }
   }
-  const uint32_t K = nkeys < (uint32_t)kTopkBlocks ? nkeys : (uint32_t)kTopkBlocks;
-  uint32_t lo = thr;
-  int ncand = sh.ncand;
-  if (K > 0 && thr == 0u) {
-    // 2. a second sweep keeps the keys >= L0, the smallest per-thread
-    // maximum: a lower bound of the K-th largest key when >= K threads hold
-    // a key (K distinct keys -- the maxima -- are >= it); else L0 = 1
-    lo = nonempty >= K ? minmax : 1u;
-    sweep(lo, false);                                      // the first sweep kept none
-    __syncthreads();
-    ncand = sh.ncand;
+  // With >= 512 nonzero maxima (>= 512 keys), a lower bound of their 512-th
+  // largest -- one digit pass -- bounds the 512-th largest key from below
+  const bool many = nz >= (uint32_t)kTopkBlocks;
+  const uint32_t lo =
+      many ? radix_select<false, false>(sh, usrc, nu, kTopkBlocks, umin, M, 0u, 1).T : 1u;
+
+  // 2. units whose maximum reaches lo (listed in the histogram space), then
+  // their keys >= lo into the candidate list; one shared atomic per warp and
+  // step
+  uint32_t* hit = sh.hist;
+  for (int64_t base = 0; base < nu; base += 8 * kTopkThreads) {
+    uint32_t mask = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t c = base + (int64_t)u * kTopkThreads + tid;
+      mask |= (uint32_t)(c < nu && usrc[c] >= lo) << u;   // lo >= 1: nonzero maxima only
+    }
+    int slot = warp_reserve(&sh.nhit, __popc(mask), lane);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (mask >> u & 1u) {
+        if (slot < kBins) hit[slot] = (uint32_t)(base + (int64_t)u * kTopkThreads + tid);
+        ++slot;
+      }
+    }
   }
-  const bool fits = ncand <= kCandCap;
+  __syncthreads();
+  const int nhit = sh.nhit;
+  if (nhit <= kBins) {
+    for (int base = 0; base < nhit; base += kTopkThreads) {
+      const int h = base + tid;
+      const int64_t g = h < nhit ? (int64_t)hit[h] : -1;
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[j] = g >= 0 ? ld_cg16(sc + kUnitKeys * g + 4 * j) : make_uint4(0, 0, 0, 0);
+      uint32_t mask = 0;                                   // bit j: key j of the unit
+#pragma unroll
+      for (int j = 0; j < kUnitKeys; ++j) {
+        const uint32_t x = g >= 0 && kUnitKeys * g + j < Vs ? u4_at(v[j >> 2], j & 3) : 0u;
+        mask |= (uint32_t)(x >= lo) << j;
+      }
+      int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
+#pragma unroll
+      for (int j = 0; j < kUnitKeys; ++j) {
+        if (mask >> j & 1u) {
+          if (slot < kCandCap) {
+            sh.cand_x[slot] = u4_at(v[j >> 2], j & 3);
+            sh.cand_i[slot] = (uint32_t)(kUnitKeys * g + j);
+          }
+          ++slot;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int ncand = sh.ncand;
+  const bool fits = nhit <= kBins && ncand <= kCandCap;
+  // K = min(512, #keys): with >= 512 nonzero maxima there are >= 512 keys;
+  // otherwise every key is a candidate (fewer than 512 units hold keys)
+  const uint32_t K = many ? (uint32_t)kTopkBlocks
+                          : (ncand < kTopkBlocks ? (uint32_t)ncand : (uint32_t)kTopkBlocks);
   const uint32_t tie_lo = 0x80000000u - (uint32_t)Vs;      // 2^31-1 - (Vs-1)
 
   if (K > 0) {
@@ -1039,7 +1077,7 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
         }
       }
     } else {
-      // fallback: select over all keys of the row
+      // fallback (many holds here, so K = 512): select over all keys of the row
       const Selected sel = radix_select<false, false>(sh, sc, Vs, K, 1u, M);
       const uint32_t T = sel.T;
       for (int64_t b0 = 0; b0 < Vs; b0 += kTopkThreads) {
@@ -1266,8 +1304,10 @@ follow_kernel(const SelectParams sp, const AttentionParams ap) {
 
 }  // namespace
 
+// [R, cols*128] score keys, then [R, cols*8] unit maxima
 size_t select_workspace_bytes(int64_t R, int64_t pt_cols) {
-  const size_t n = (size_t)R * (size_t)pt_cols * kCmpPageKeys * sizeof(uint32_t);
+  const size_t n = (size_t)R * (size_t)pt_cols * (kCmpPageKeys + kCmpPageKeys / kUnitKeys) *
+                   sizeof(uint32_t);
   return (n + 255) & ~(size_t)255;
 }
 
@@ -1361,6 +1401,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     c.qpos = p.qpos + r0;
     c.out = p.out + (int64_t)r0 * p.out_stride0;
     c.scores = p.scores + (int64_t)r0 * p.vcap;
+    c.umax = p.umax + (int64_t)r0 * (p.vcap / kUnitKeys);
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
     if (c.key_fp8)
@@ -1392,6 +1433,7 @@ cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a
     c.qpos = p.qpos + r0;
     c.out = p.out + (int64_t)r0 * p.out_stride0;
     c.scores = p.scores + (int64_t)r0 * p.vcap;
+    c.umax = p.umax + (int64_t)r0 * (p.vcap / kUnitKeys);
     AttentionParams ac = a;
     ac.R = c.R;
     ac.q = a.q + (int64_t)r0 * kAttHeads * kAttDim;

@@ -66,7 +66,9 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_queries(lib):
     assert lib.qsa_select_workspace_bytes(0, 10) == 0
-    assert lib.qsa_select_workspace_bytes(256, 256) == 256 * 256 * 128 * 4
+    # per row: a 32-bit key per block (128 per page-table column) and the
+    # largest key of each run of 16 blocks
+    assert lib.qsa_select_workspace_bytes(256, 256) == 256 * 256 * (128 + 8) * 4
     assert lib.qsa_select_workspace_bytes(1, 1) % 256 == 0
     assert lib.qsa_attention_workspace_bytes(0, 2051) == 0
     a = lib.qsa_attention_workspace_bytes(256, 2051)
