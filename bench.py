@@ -399,6 +399,9 @@ def run_ours(args, world, rank, local):
     if not args.no_fp8:
         fp8 = fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak)
     meta = metadata_timing(args, R, world, dev, stream, w.cmp_page_table, w.seq_lens)
+    r1 = None
+    if not args.no_r1 and args.workload == 4:
+        r1 = r1_latency(args, dev, stream)
     spec = None
     if not args.no_spec and args.workload == 4:
         spec = spec_variant(args, R, world, rank, dev, stream, peak)
@@ -447,6 +450,7 @@ def run_ours(args, world, rank, local):
         "fused_select_attend": fused,
         "fp8_compressed_cache": fp8,
         "metadata_builder": meta,
+        "latency_R1": r1,
         "speculative_decode": spec,
         "paged_mqa_indexer": indexer,
         "gpu_launches": 4 * K,
@@ -553,6 +557,67 @@ def _time_calls(fn, n, stream, dev, world):
     torch.cuda.synchronize(dev)
     barrier(world)
     return max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+
+
+def r1_latency(args, dev, stream):
+    """Single-row decode latency on the pages' two R=1 cases (519 tokens over
+    two compressed pages; 9215 tokens, 2303 blocks in a pool of 8192 pages):
+    microseconds per call of selection, attention, the two-call step and the
+    one-call step.  Before every timed call a 256 MiB buffer is written so
+    the call starts with its inputs out of L2; median and min of 50 calls."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for cfg in (0, 1):
+        w = W.config(cfg, device=dev)
+        idx = torch.empty((1, 2051), dtype=torch.int32, device=dev)
+        o = torch.empty((1, 3, 256), dtype=torch.float16, device=dev)
+        cols = w.cmp_page_table.shape[1]
+        sws = torch.empty(qsa.qsa_select_workspace_bytes(1, cols), dtype=torch.uint8, device=dev)
+        aws = torch.empty(qsa.qsa_attention_workspace_bytes(1, 2051), dtype=torch.uint8,
+                          device=dev)
+        fws = torch.empty(qsa.qsa_select_attend_workspace_bytes(1, cols), dtype=torch.uint8,
+                          device=dev)
+
+        def sel():
+            qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, w.cmp_page_table,
+                                        w.token_to_request, w.seq_lens, w.query_positions,
+                                        out=idx, workspace=sws, stream=stream)
+
+        def att():
+            qsa.qsa_sparse_attention(w.q_attn, w.k_view, w.v_view, w.kv_page_table,
+                                     w.token_to_request, idx, out=o, workspace=aws,
+                                     stream=stream)
+
+        def both():
+            sel()
+            att()
+
+        def fused():
+            qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                                  w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                                  w.kv_page_table, indices=idx, out=o, workspace=fws,
+                                  stream=stream)
+
+        res = {}
+        for name, fn in (("select", sel), ("attend", att), ("two_call_step", both),
+                         ("one_call_step", fused)):
+            for _ in range(5):
+                fn()
+            ts = []
+            for _ in range(50):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            res[name] = {"us_median": statistics.median(ts), "us_min": min(ts)}
+        out[W.CONFIG_NAMES[cfg]] = res
+    return out
 
 
 def metadata_timing(args, R, world, dev, stream, cmp_pt, seq):
@@ -723,6 +788,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8-E4M3 compressed-cache measurement")
+    ap.add_argument("--no-r1", action="store_true",
+                    help="skip the single-row latency measurement (workloads 0 and 1)")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the one-call select+attend (qsa_select_attend) measurement")
     ap.add_argument("--no-spec", action="store_true",

@@ -317,7 +317,7 @@ qsa_status qsa_sparse_attention(
       if (overlaps(e, s)) return QSA_ERR_ALIAS;
   }
   p.part = static_cast<float*>(workspace);
-  p.nsplit = qsa::attention_splits(index_width);
+  p.nsplit = qsa::attention_splits(num_rows, index_width);
   const cudaError_t e = qsa::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

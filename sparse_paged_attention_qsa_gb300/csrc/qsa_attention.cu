@@ -7,9 +7,9 @@
 // [R,2051] int32 with holes and duplicates; caller-owned output.
 //
 // Split-width flash decoding (device code in qsa_attn_impl.cuh):
-//   attn_partial_kernel  grid (splits, R); each CTA takes kSplit = 256
-//                        consecutive entries of one row's index list (a
-//                        2051-wide row: 9 CTAs); each warp compacts its 64
+//   attn_partial_kernel  grid (splits, R); each CTA takes 256 consecutive
+//                        entries of one row's index list (64 when the batch
+//                        has at most 16 rows); each warp compacts its
 //                        entries to the valid tokens and walks them 8 at a
 //                        time (8 KiB of K/V in flight per warp).  Logits
 //                        (mixed-precision FMA, fp16 operands, binary32
@@ -29,22 +29,29 @@ namespace {
 
 using attn::kPartFloats;
 
-#ifndef QSA_ATT_SPLIT
-#define QSA_ATT_SPLIT 256
-#endif
-constexpr int kSplit = QSA_ATT_SPLIT;  // index entries per CTA
 constexpr int kAttWarps = 4;
-constexpr int kWarpEntries = kSplit / kAttWarps;   // 64 entries per warp
 constexpr int kAttThreads = kAttWarps * 32;
-constexpr int kMaxSplits = (kOutWidth + kSplit - 1) / kSplit;   // 9
+// Entries of a row's index list per CTA: 256 for batches of many rows (each
+// warp walks 64 entries, 8 batches: the CTA's fixed costs -- the dependent
+// index -> page-table -> K/V loads before streaming and the merge after it
+// -- are amortised; 128 entries: 0.106 ms on 256 x 2048 rows, 256: 0.101,
+// 512: 0.116 with too few CTAs to fill the GPU evenly), 64 for small batches
+// (each warp walks 16 entries, 2 batches: a single row's 2051 entries go to
+// 33 CTAs, so the row's latency is a couple of memory round trips).
+constexpr int kSplitLarge = 256;
+constexpr int kSplitSmall = 64;
+constexpr int kSmallRows = 16;     // batches of at most this many rows take the small split
+constexpr int kMaxSplitsLarge = (kOutWidth + kSplitLarge - 1) / kSplitLarge;   // 9
+constexpr int kMaxSplitsSmall = (kOutWidth + kSplitSmall - 1) / kSplitSmall;   // 33
 
-// One CTA = kSplit consecutive entries of one row's index list.  256 entries
-// per CTA amortise the CTA's fixed costs -- the dependent index -> page-table
-// -> K/V loads before streaming and the merge after it -- over 8 batches per
-// warp (128 entries: 0.106 ms on 256 x 2048 rows, 256: 0.101, 512: 0.116 with
-// too few CTAs to fill the GPU evenly).
+int split_entries(int64_t R) { return R <= kSmallRows ? kSplitSmall : kSplitLarge; }
+
+// One CTA = kSplit consecutive entries of one row's index list, kSplit / 4
+// per warp.
+template <int kSplit>
 __global__ void __launch_bounds__(kAttThreads)
 attn_partial_kernel(const AttentionParams p) {
+  constexpr int kWarpEntries = kSplit / kAttWarps;
   const int split = blockIdx.x;
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
@@ -74,6 +81,7 @@ attn_partial_kernel(const AttentionParams p) {
 
 // One CTA per row: log-sum-exp merge of the row's split partials; thread d
 // handles dim d of every head.
+template <int kMaxSplits>
 __global__ void __launch_bounds__(kAttDim)
 attn_combine_kernel(const AttentionParams p) {
   __shared__ attn::CombineSmem<kMaxSplits> sm;
@@ -85,13 +93,14 @@ attn_combine_kernel(const AttentionParams p) {
 
 }  // namespace
 
-int attention_splits(int64_t width) {
-  const int64_t s = (width + kSplit - 1) / kSplit;
+int attention_splits(int64_t R, int64_t width) {
+  const int e = split_entries(R);
+  const int64_t s = (width + e - 1) / e;
   return s > 0 ? (int)s : 1;
 }
 
 size_t attention_workspace_bytes(int64_t R, int64_t width) {
-  const size_t n = (size_t)R * (size_t)attention_splits(width) * kPartFloats * sizeof(float);
+  const size_t n = (size_t)R * (size_t)attention_splits(R, width) * kPartFloats * sizeof(float);
   return (n + 255) & ~(size_t)255;
 }
 
@@ -101,9 +110,16 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream) {
   // a programmatic dependent of whatever ran before on the stream: after the
   // selection's top-k (which triggers at its start) the launch and CTA
   // scheduling overlap the top-k's tail; the kernel waits before any read
-  cudaError_t e = launch_after(attn_partial_kernel, grid, dim3(kAttThreads), 0, stream, p);
+  const bool small = split_entries(p.R) == kSplitSmall;
+  cudaError_t e = small ? launch_after(attn_partial_kernel<kSplitSmall>, grid,
+                                       dim3(kAttThreads), 0, stream, p)
+                        : launch_after(attn_partial_kernel<kSplitLarge>, grid,
+                                       dim3(kAttThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
-  return launch_after(attn_combine_kernel, dim3(p.R), dim3(kAttDim), 0, stream, p);
+  return small ? launch_after(attn_combine_kernel<kMaxSplitsSmall>, dim3(p.R), dim3(kAttDim), 0,
+                              stream, p)
+               : launch_after(attn_combine_kernel<kMaxSplitsLarge>, dim3(p.R), dim3(kAttDim), 0,
+                              stream, p);
 }
 
 }  // namespace qsa

@@ -93,17 +93,18 @@ __device__ __forceinline__ void load_query(const AttentionParams& p, int r, int 
 
 // Resolve entries [j0, j0 + kEntries) of row r's index list (those < width)
 // to tokens (page*512 + slot), dropping holes and unmapped pages, compacted
-// in order into tok[]; returns how many.
+// in order into tok[]; returns how many.  kEntries is 16 or a multiple of 32.
 template <int kEntries>
 __device__ __forceinline__ int resolve_entries(const AttentionParams& p, int r, int req, bool rok,
                                                int64_t j0, uint32_t* tok, int lane) {
+  static_assert(kEntries == 16 || kEntries % 32 == 0, "entries per warp");
   int nvalid = 0;
 #pragma unroll
   for (int c = 0; c < kEntries; c += 32) {
     const int64_t j = j0 + c + lane;
     bool valid = false;
     uint32_t t = 0;
-    if (rok && j < p.width) {
+    if (rok && c + lane < kEntries && j < p.width) {
       const int32_t i = p.idx[(int64_t)r * p.idx_stride0 + j];
       if (i >= 0) {
         const int64_t col = i >> 9;

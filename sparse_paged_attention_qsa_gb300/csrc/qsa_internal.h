@@ -110,6 +110,6 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream);
 // fused_sync_bytes(min(R, kFusedMaxRows)) bytes.
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream);
-int attention_splits(int64_t width);
+int attention_splits(int64_t R, int64_t width);
 
 }  // namespace qsa
