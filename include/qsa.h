@@ -236,6 +236,8 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * the stream: the score kernel on most SMs, and a follower kernel
  * (launched as its programmatic dependent) on the others, which takes each
  * row's top-k once the row's keys are scored and then the row's attention.
+ * A batch of at most 16 rows has little scoring to overlap and runs the
+ * kernels of the two separate calls instead (same results).
  * The follower waits on counters the score kernel publishes; every wait
  * gives up after 1 s (QSA_DERR_TIMEOUT in *error_word; the outputs are then
  * incomplete), so a fault can never hang the GPU.  Calls that share a

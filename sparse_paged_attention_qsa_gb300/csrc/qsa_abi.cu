@@ -8,6 +8,7 @@
 #include "qsa.h"
 #include "qsa_internal.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -201,7 +202,11 @@ FusedLayout fused_layout(int64_t num_rows, int64_t cmp_pt_cols) {
   const auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
   FusedLayout l;
   l.part = up(qsa::select_workspace_bytes(num_rows, cmp_pt_cols));
-  l.sync = l.part + up((size_t)rows * qsa::kFusedSplits *
+  // partials of the follower's 512-entry items, or of the split attention
+  // kernels when a small batch takes the two-kernel route
+  const int64_t splits = std::max<int64_t>(qsa::kFusedSplits,
+                                           qsa::attention_splits(rows, qsa::kOutWidth));
+  l.sync = l.part + up((size_t)rows * splits *
                        (qsa::kAttHeads * 2 + qsa::kAttHeads * kAttDim) * sizeof(float));
   l.total = l.sync + up(qsa::fused_sync_bytes(rows));
   return l;

@@ -1175,6 +1175,7 @@ constexpr int kFollowWarps = kFollowThreads / 32;
 static_assert(kFusedSplit == kFollowWarps * 32, "one 32-entry run per warp and item");
 constexpr int kItemLag = 4;
 constexpr int kFollowSMs = 40;                          // SMs the score kernel leaves free
+constexpr int kFusedMinRows = 16;   // batches of at most this many rows take the split kernels
 
 struct FollowAttnSmem {
   attn::MergeSmem<kFollowWarps> merge;
@@ -1417,6 +1418,18 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
+  if (p.R <= kFusedMinRows) {
+    // a small batch has little scoring to overlap: the split kernels (selection,
+    // then attention over its output) finish sooner
+    cudaError_t e = launch_select(p, stream);
+    if (e != cudaSuccess) return e;
+    AttentionParams ac = a;
+    ac.idx = p.out;
+    ac.idx_stride0 = p.out_stride0;
+    ac.width = kOutWidth;
+    ac.nsplit = attention_splits(p.R, kOutWidth);
+    return launch_attention(ac, stream);
+  }
   DeviceInfo* di = nullptr;
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return e;

@@ -5,11 +5,13 @@ indices ("vLLM: integrate FP16 packed QSA extension", Summary and "Exact
 contracts"/Selection and Attention; the pages' tie, tail, saturation and
 multi-request cases).
 
-The fused path overlaps the attention of early rows with the scoring of
-later ones (a score kernel and a follower kernel that waits on per-row
-counters), so these tests also cover its row chunks (more than 1024 rows),
-speculative rows that share a request, bad ids, and repeated calls on a
-dirty workspace.  Tolerance as in test_gpu_attention.py.
+A batch of more than 16 rows runs a score kernel and a follower kernel
+that waits on per-row counters (the attention of early rows overlaps the
+scoring of later ones); a smaller batch runs the two calls' kernels.  The
+edge cases run both ways (the row list repeated past 16 rows), and the
+tests also cover row chunks (more than 1024 rows), speculative rows that
+share a request, and repeated calls on a dirty workspace.  Tolerance as in
+test_gpu_attention.py.
 """
 import numpy as np
 import pytest
@@ -76,17 +78,24 @@ def test_fused_matches_two_call_path():
     assert np.abs(got_out - out2.float().cpu().numpy()).max() <= TOL
 
 
+def _rows(lens, big):
+    """The row list, repeated past 16 rows when the follower route is wanted."""
+    return lens * (17 // len(lens) + 1) if big else lens
+
+
+@pytest.mark.parametrize("big", [False, True])
 @pytest.mark.parametrize("lens", [[0, 1, 3, 4, 7, 515, 516, 519, 1027], [2051, 2053, 9215, 131072]])
-def test_fused_short_empty_and_saturated_rows(lens):
-    w = W.build("edge", lens, seed=sum(lens) % 1000 + 3, device=DEV)
+def test_fused_short_empty_and_saturated_rows(lens, big):
+    w = W.build("edge", _rows(lens, big), seed=sum(lens) % 1000 + 3, device=DEV)
     _, got_out, gerr, oerr = _check(w)
     assert gerr == oerr == 0
     assert (got_out[0] == 0).all() if lens[0] == 0 else True   # no valid entry -> zeros
 
 
-def test_fused_heavy_ties_and_duplicate_pages():
-    w = W.build("ties", [6003, 4099, 30001, 515, 131072], distinct_keys=2, dup_mapping=True,
-                seed=31, device=DEV)
+@pytest.mark.parametrize("big", [False, True])
+def test_fused_heavy_ties_and_duplicate_pages(big):
+    w = W.build("ties", _rows([6003, 4099, 30001, 515, 131072], big), distinct_keys=2,
+                dup_mapping=True, seed=31, device=DEV)
     _check(w)
 
 
@@ -108,12 +117,14 @@ def test_fused_speculative_rows_share_pages():
     assert gerr == oerr == 0
 
 
-def test_fused_bad_ids_set_error_bits():
-    w = W.build("bad", [3000, 3000, 3000, 9000], seed=36, device=DEV)
+@pytest.mark.parametrize("big", [False, True])
+def test_fused_bad_ids_set_error_bits(big):
+    w = W.build("bad", _rows([3000, 3000, 3000, 9000], big), seed=36, device=DEV)
     pt = w.cmp_page_table.clone()
     pt[1, 2] = w.cmp_cache.shape[0] + 5         # compressed page beyond the pool
     pt[3, 0] = -1                               # unmapped compressed page
-    t2r = torch.tensor([0, 1, 9, 3], dtype=torch.int32, device=DEV)   # row 2: no request
+    t2r = torch.arange(w.R, dtype=torch.int32, device=DEV)
+    t2r[2] = w.R + 9                            # row 2: no such request
     got_idx, got_out, gerr, oerr = _check(w, pt=pt, t2r=t2r)
     assert gerr == oerr == (qsa.DERR_REQUEST | qsa.DERR_CMP_PAGE)
     assert (got_idx[2] == -1).all() and (got_out[2] == 0).all()
@@ -134,8 +145,9 @@ def test_fused_more_rows_than_one_launch():
     assert gerr == 0
 
 
-def test_fused_repeat_calls_on_dirty_workspace():
-    w = W.config(1, device=DEV)
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_fused_repeat_calls_on_dirty_workspace(cfg):
+    w = W.config(cfg, device=DEV)
     a_idx, a_out, _ = _fused(w)
     need = qsa.qsa_select_attend_workspace_bytes(w.R, w.cmp_page_table.shape[1])
     ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)   # counters start dirty
