@@ -110,7 +110,7 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream) {
   // a programmatic dependent of whatever ran before on the stream: after the
   // selection's top-k (which triggers at its start) the launch and CTA
   // scheduling overlap the top-k's tail; the kernel waits before any read
-  const bool small = split_entries(p.R) == kSplitSmall;
+  const bool small = p.R <= kSmallRows;
   cudaError_t e = small ? launch_after(attn_partial_kernel<kSplitSmall>, grid,
                                        dim3(kAttThreads), 0, stream, p)
                         : launch_after(attn_partial_kernel<kSplitLarge>, grid,

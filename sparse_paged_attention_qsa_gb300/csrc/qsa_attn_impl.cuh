@@ -93,33 +93,36 @@ __device__ __forceinline__ void load_query(const AttentionParams& p, int r, int 
 
 // Resolve entries [j0, j0 + kEntries) of row r's index list (those < width)
 // to tokens (page*512 + slot), dropping holes and unmapped pages, compacted
-// in order into tok[]; returns how many.  kEntries is 16 or a multiple of 32.
+// in order into tok[]; returns how many.  kEntries is 16 or a multiple of
+// 32.  All index loads are issued before the page-table loads that depend on
+// them, so the list costs two memory round trips however long it is.
 template <int kEntries>
 __device__ __forceinline__ int resolve_entries(const AttentionParams& p, int r, int req, bool rok,
                                                int64_t j0, uint32_t* tok, int lane) {
   static_assert(kEntries == 16 || kEntries % 32 == 0, "entries per warp");
+  constexpr int kIter = (kEntries + 31) / 32;
+  int32_t iv[kIter];
+#pragma unroll
+  for (int c = 0; c < kIter; ++c) {
+    const int64_t j = j0 + 32 * c + lane;
+    iv[c] = rok && 32 * c + lane < kEntries && j < p.width
+                ? p.idx[(int64_t)r * p.idx_stride0 + j] : -1;
+  }
+  int32_t pg[kIter];
+#pragma unroll
+  for (int c = 0; c < kIter; ++c) {
+    const int64_t col = iv[c] >> 9;
+    pg[c] = iv[c] >= 0 && col < p.pt_cols ? p.pt[(int64_t)req * p.pt_stride0 + col] : -1;
+  }
   int nvalid = 0;
 #pragma unroll
-  for (int c = 0; c < kEntries; c += 32) {
-    const int64_t j = j0 + c + lane;
-    bool valid = false;
-    uint32_t t = 0;
-    if (rok && c + lane < kEntries && j < p.width) {
-      const int32_t i = p.idx[(int64_t)r * p.idx_stride0 + j];
-      if (i >= 0) {
-        const int64_t col = i >> 9;
-        int32_t pg = -1;
-        if (col < p.pt_cols) pg = p.pt[(int64_t)req * p.pt_stride0 + col];
-        if (pg >= 0 && pg < p.num_pages) {
-          valid = true;
-          t = (uint32_t)pg * kKvPageTokens + (uint32_t)(i & 511);
-        } else {
-          report(p.err, kErrKvPage);
-        }
-      }
-    }
+  for (int c = 0; c < kIter; ++c) {
+    const bool valid = iv[c] >= 0 && pg[c] >= 0 && pg[c] < p.num_pages;
+    if (iv[c] >= 0 && !valid) report(p.err, kErrKvPage);
     const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-    if (valid) tok[nvalid + __popc(vmask & ((1u << lane) - 1u))] = t;
+    if (valid)
+      tok[nvalid + __popc(vmask & ((1u << lane) - 1u))] =
+          (uint32_t)pg[c] * kKvPageTokens + (uint32_t)(iv[c] & 511);
     nvalid += __popc(vmask);
   }
   __syncwarp();
@@ -214,20 +217,12 @@ struct MergeSmem {
   float acc[kWarps][kAttHeads][kAttDim];
 };
 
-// Merge the CTA's kWarps warp states into one partial (m, l, acc[256]) per
-// head at `part` (kPartFloats floats).  Every thread of the CTA calls this;
-// it ends without a barrier after its reads of shared memory.
+// Merge the kWarps warp states stored in sm into one partial (m, l,
+// acc[256]) per head at `part` (kPartFloats floats).  Every thread of the
+// CTA calls this after the warps stored their states; it starts with a block
+// barrier and ends without one, after its reads of shared memory.
 template <int kWarps>
-__device__ __forceinline__ void merge_warps(const WarpState& st, MergeSmem<kWarps>& sm, float* part,
-                                            int tid, int warp, int lane) {
-#pragma unroll
-  for (int h = 0; h < kAttHeads; ++h)
-#pragma unroll
-    for (int d = 0; d < 8; ++d) sm.acc[warp][h][8 * lane + d] = st.acc[h][d];
-  if (lane < kAttHeads) {
-    sm.m[warp][lane] = st.m_run;
-    sm.l[warp][lane] = st.l_run;
-  }
+__device__ __forceinline__ void merge_stored(MergeSmem<kWarps>& sm, float* part, int tid) {
   __syncthreads();
   for (int o = tid; o < kAttHeads * kAttDim; o += kWarps * 32) {
     const int h = o / kAttDim, d = o % kAttDim;
@@ -249,6 +244,21 @@ __device__ __forceinline__ void merge_warps(const WarpState& st, MergeSmem<kWarp
       part[kAttHeads + h] = Lsum;
     }
   }
+}
+
+// Merge the CTA's kWarps warp states (WarpState layout) into one partial.
+template <int kWarps>
+__device__ __forceinline__ void merge_warps(const WarpState& st, MergeSmem<kWarps>& sm, float* part,
+                                            int tid, int warp, int lane) {
+#pragma unroll
+  for (int h = 0; h < kAttHeads; ++h)
+#pragma unroll
+    for (int d = 0; d < 8; ++d) sm.acc[warp][h][8 * lane + d] = st.acc[h][d];
+  if (lane < kAttHeads) {
+    sm.m[warp][lane] = st.m_run;
+    sm.l[warp][lane] = st.l_run;
+  }
+  merge_stored<kWarps>(sm, part, tid);
 }
 
 template <int kMaxSplits>
