@@ -448,7 +448,10 @@ def run_ours(args, world, rank, local):
         rate0, _ = oracle_rate(sample, 2 * len(sample.rows), threads)   # calibration
         n = max(2 * len(sample.rows), int(rate0 * 10.0))                 # about 10 s of rows
         rate, dt = oracle_rate(sample, n, threads)
+        n1 = max(2, int(rate / threads * 3.0))                           # about 3 s on one core
+        rate1, _ = oracle_rate(sample, n1, 1)
         cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "single_thread_value": rate1,
                "sample": f"{n} decode rows (select+attend) over {len(sample.rows)} rows of "
                          f"this workload, plain C oracle on {threads} threads, {dt:.1f} s wall"}
 
