@@ -93,6 +93,20 @@ def test_attention_config4_full_size_sampled_rows():
     assert np.isfinite(got).all()
 
 
+@pytest.mark.parametrize("R", [16, 17, 40])
+def test_attention_batch_sizes_around_the_split_switch(R):
+    # batches of up to 16 rows take 64-entry splits, larger ones 256-entry
+    # splits: premade lists with holes and duplicates, every width, bad ids
+    w = _lists(R, [0, 1, 32, 1024, 2051, 1500, 77], 3000, seed=60 + R)
+    pt = w.kv_page_table.clone()
+    pt[1, 0] = -1                                   # an unmapped K/V page
+    t2r = torch.arange(R, dtype=torch.int32, device=DEV)
+    t2r[R - 1] = R + 5                              # the last row has no request
+    got, gerr, oerr, _ = _check(w, w.indices, pt=pt, t2r=t2r)
+    assert gerr == oerr
+    assert (got[R - 1] == 0).all()
+
+
 def test_attention_single_index_exact():
     w = W.build("one", [5000, 5000], seed=3, device=DEV)
     idx = torch.full((2, 2051), -1, dtype=torch.int32, device=DEV)
