@@ -19,10 +19,12 @@
 //   warps 1, 18  MMA issuers, alternate tiles each: one lane issues four
 //           tcgen05.mma kind::f8f6f4 (M = 128 tokens, N = next_n x heads,
 //           K = 32 each) per tile into a TMEM accumulator of its own
-//           (tile n uses accumulator n % 4, or n % 2 when N = 256), commits
-//           to the accumulator's barrier, and refills nothing until that
-//           accumulator's previous tile is consumed -- then releases that
-//           tile's stage to the producer; warp 1 owns the TMEM allocation;
+//           (tile n uses accumulator n % 4, or n % 2 when N = 256) once that
+//           accumulator's previous tile is consumed, and commits to the
+//           accumulator's barrier and to the stage's: a stage is refilled
+//           as soon as its MMAs have read the values and the epilogue warps
+//           have read the scales and descriptor; warp 1 owns the TMEM
+//           allocation;
 //   warps 2-17  epilogue in four groups of four warps (one warp per TMEM
 //           lane quarter); group g takes the tiles of accumulator g, so no
 //           warp waits on a barrier phase ahead of its predecessor: each
@@ -312,7 +314,9 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       bar_init(bar_full + 8 * s, 1);
-      bar_init(bar_empty + 8 * s, 1);    // the MMA thread, once the tile's epilogue is done
+      // the tile's MMAs done reading the values (tcgen05.commit) + the four
+      // epilogue warps done reading the scales and the descriptor
+      bar_init(bar_empty + 8 * s, 1 + 4);
     }
     for (int a = 0; a < kMaxAcc; ++a) {
       bar_init(bar_accf + 8 * a, 1);
@@ -528,18 +532,16 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
     if (lane == 0 && g < I) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
       int s = g, round = 0, a = g, around = 0;          // ring / accumulator position of tile n
-      uint32_t held = 0;                                // stage of the tile in each accumulator (8 bits each)
       uint32_t seen_q = 0xffffffffu;                    // query slot and phase last waited for
       for (int64_t n = g;; n += I) {
         // accumulator a free again: the epilogue is done with the tile that
-        // used it, so that tile's stage (values, scales) can be refilled
+        // used it
         if (around > 0) {
           if (!wait_phase(bar_acce + 8 * a, (uint32_t)((around - 1) & 1))) {
             *abort_flag = 1;
             report(p.err, kErrTimeoutBit);
             break;
           }
-          bar_arrive(bar_empty + 8 * ((held >> (8 * a)) & 0xffu));
         }
         // tile n's data, or the producer's end marker covering tile n
         int state = test_wait(bar_full + 8 * s, (uint32_t)(round & 1)) ? 1 : 0;
@@ -555,7 +557,6 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
           break;
         }
         if (state == 2 || *abort_flag) break;
-        held = (held & ~(0xffu << (8 * a))) | ((uint32_t)s << (8 * a));
         const TileDesc d = desc[s];
         if (d.b < 0) break;                             // the end marker's stage
         const int qs = (int)(d.qinfo & 1u);
@@ -575,6 +576,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int k = 0; k < kDim / 32; ++k) tc_mma(dt, da + 2 * k, db + 2 * k, idesc, k);
         tc_commit(bar_accf + 8 * a);
+        tc_commit(bar_empty + 8 * s);           // the values may be refilled once read
         if (d.qinfo & 4u) tc_commit(bar_qempty + 8 * qs);
         last_issued = n;
         s += I;
@@ -619,8 +621,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       }
       if (n >= *end_tile || *abort_flag) break;
       // the stage's full barrier has completed for this tile (its refill
-      // waits for this tile's epilogue): waiting on it again makes the
-      // producer's descriptor and the copied scales visible here
+      // waits for this group's four warps, below): waiting on it again makes
+      // the producer's descriptor and the copied scales visible here
       if (!wait_phase(bar_full + 8 * s, (uint32_t)(round & 1))) {
         *abort_flag = 1;
         report(p.err, kErrTimeoutBit);
@@ -643,6 +645,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
           reinterpret_cast<const float*>(gbase + qslots + (size_t)qs * p.qslot_bytes + wOff);
       const bool missing = (d.missing >> (row >> p.bs_log2)) & 1u;
       const int64_t t = (int64_t)d.tile * kTile + row;
+      __syncwarp();                              // every lane has its scale and the descriptor
+      if (lane == 0) bar_arrive(bar_empty + 8 * s);   // the stage may be refilled
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N);
       float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
