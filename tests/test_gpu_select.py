@@ -100,6 +100,13 @@ def test_select_long_rows_heavy_ties(distinct):
     _check(w)
 
 
+def test_select_rows_longer_than_the_staged_unit_maxima():
+    # 300003 tokens: 75000 blocks, 4688 unit maxima (more than the 4096 the
+    # top-k stages in shared memory: it reads them from the workspace)
+    w = W.build("verylong", [300003, 262147, 5000], seed=15, device=DEV)
+    _check(w)
+
+
 def test_select_all_zero_scores_long_row():
     # every key equals bits(+0)+1: 32768 ties, kept in block order
     w = W.build("zeros_long", [131072], seed=14, device=DEV)
