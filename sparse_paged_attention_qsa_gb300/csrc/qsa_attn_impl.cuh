@@ -1,5 +1,5 @@
 // qsa_attn_impl.cuh -- device code of the sparse attention shared by the
-// split kernels (qsa_attention.cu) and the fused select -> attend path
+// attention kernels (qsa_attention.cu) and the fused select -> attend path
 // (qsa_select.cu).
 //
 // "vLLM: integrate FP16 packed QSA extension", Summary (exact-packed
@@ -10,9 +10,10 @@
 // FP32 accumulation; FP16 output, round to nearest even; no valid entry
 // gives 0.
 //
-// Split-width flash decoding: a warp walks a run of the index list and keeps
-// a running (m, l, acc) per head in base 2; the warps of a CTA merge into one
-// partial per split; one pass per row merges the splits by log-sum-exp.
+// Flash decoding over pieces of the index list: a warp walks a run of the
+// list and keeps a running (m, l, acc) per head in base 2; the warps of a
+// CTA merge into one partial per piece; one pass per row merges the pieces
+// by log-sum-exp.
 #pragma once
 
 #include "qsa_internal.h"
@@ -26,46 +27,9 @@ namespace attn {
 constexpr int kBatch = 8;            // tokens per warp step
 constexpr int kPartFloats = kAttHeads * 2 + kAttHeads * kAttDim;   // m[3], l[3], acc[3][256]
 
-// acc + a*b with fp16 operands and a binary32 accumulator
-__device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float c) {
-  float d;
-  if (hi)
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
-        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  else
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
-        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-
-__device__ __forceinline__ void to_f32x8(const uint4 v, float* f) {
-  const float2 a = h2f2(v.x), b = h2f2(v.y), c = h2f2(v.z), d = h2f2(v.w);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-}
-
-// Sum 32 per-lane values over the warp, reduce-scatter style: on return
-// x[0] of lane l holds the warp-wide sum of value l (31 shuffles).
-__device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane) {
-#pragma unroll
-  for (int level = 0; level < 5; ++level) {
-    const int half = 16 >> level;            // values kept after this level
-    const int bit = 16 >> level;             // partner lane distance
-    const bool upper = (lane & bit) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? x[i] : x[i + half];
-      const float keep = upper ? x[i + half] : x[i];
-      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-    }
-  }
-  return x[0];
-}
-
-// A warp's running softmax state: lane h < 3 holds head h's m and l (base 2);
-// lane l holds dims [8l, 8l+8) of each head's accumulator.
+// A warp's running softmax state: lane h < 3 holds head h's m and l (base 2;
+// lanes 4h..4h+3 while a walk is under way, see attend_tokens_mma); lane l
+// holds dims [8l, 8l+8) of each head's accumulator.
 struct WarpState {
   float m_run, l_run;
   float acc[kAttHeads][8];
@@ -80,17 +44,6 @@ __device__ __forceinline__ void init_state(WarpState& st) {
     for (int d = 0; d < 8; ++d) st.acc[h][d] = 0.f;
 }
 
-// query dims [8*lane, 8*lane+8) of each head of row r, fp16 pairs
-__device__ __forceinline__ void load_query(const AttentionParams& p, int r, int lane,
-                                           uint32_t (&qh)[kAttHeads][4]) {
-  const uint4* qp = reinterpret_cast<const uint4*>(p.q + (int64_t)r * kAttHeads * kAttDim);
-#pragma unroll
-  for (int h = 0; h < kAttHeads; ++h) {
-    const uint4 v = qp[h * 32 + lane];
-    qh[h][0] = v.x; qh[h][1] = v.y; qh[h][2] = v.z; qh[h][3] = v.w;
-  }
-}
-
 // Resolve entries [j0, j0 + kEntries) of row r's index list (those < width)
 // to tokens (page*512 + slot), dropping holes and unmapped pages, compacted
 // in order into tok[]; returns how many.  kEntries is 16 or a multiple of
@@ -103,11 +56,12 @@ __device__ __forceinline__ int resolve_entries(const AttentionParams& p, int r, 
   constexpr int kIter = (kEntries + 31) / 32;
   int32_t iv[kIter];
 #pragma unroll
-  for (int c = 0; c < kIter; ++c) {
+  for (int c = 0; c < kIter; ++c) {   // issued without waiting for the request id
     const int64_t j = j0 + 32 * c + lane;
-    iv[c] = rok && 32 * c + lane < kEntries && j < p.width
-                ? p.idx[(int64_t)r * p.idx_stride0 + j] : -1;
+    iv[c] = 32 * c + lane < kEntries && j < p.width ? p.idx[(int64_t)r * p.idx_stride0 + j] : -1;
   }
+#pragma unroll
+  for (int c = 0; c < kIter; ++c) iv[c] = rok ? iv[c] : -1;
   int32_t pg[kIter];
 #pragma unroll
   for (int c = 0; c < kIter; ++c) {
@@ -129,85 +83,187 @@ __device__ __forceinline__ int resolve_entries(const AttentionParams& p, int r, 
   return nvalid;
 }
 
-// Walk tokens tok[0..n) kBatch at a time: lane l owns dims [8l, 8l+8) of K
-// and V, so a token's 1 KiB (K then V) is two coalesced 512-byte warp loads
-// and a batch keeps 8 KiB in flight.  The 24 head logits of a batch are
-// reduced with one reduce-scatter, after which lane l holds token l/4, head
-// l%4 (head 3 is padding); the online softmax runs in base 2 with one exp2
-// per lane per batch.
-__device__ __forceinline__ void attend_tokens(const AttentionParams& p, const uint32_t* tok, int n,
-                                              const uint32_t (&qh)[kAttHeads][4], WarpState& st,
-                                              int lane) {
-  const int hh = lane & 3;         // head of this lane's logit after the reduce
-  for (int b0 = 0; b0 < n; b0 += kBatch) {
-    uint4 kr[kBatch], vr[kBatch];
+// --- tensor-core logits --------------------------------------------------------
+//
+// The batch's 3 x 8 logits as one warp-level MMA chain, Q (16 rows: the 3
+// heads, zero padding) x K^T (8 tokens): 16 mma.m16n8k16 (fp16 operands,
+// binary32 accumulation) over the 256 dims.  A dot product does not depend
+// on the order of its dims, so each lane takes a fixed set of 64 dims of its
+// token -- lane l (token l/4, c = l%4) dims 32i + 8c .. 32i + 8c + 7, i < 8:
+// four lanes read 64 contiguous bytes of a token's K per load -- and slice
+// (i, u) of the MMA chain maps the fragment's k = 2c + {0,1} to dims
+// 32i + 8c + 4u + {0,1} and k = 2c + 8 + {0,1} to 32i + 8c + 4u + 2 + {0,1},
+// in the K operand and, through QFrag, in the Q operand alike.  The
+// accumulator fragment then holds in lane l the logits of head l/4 (rows
+// >= 3 are padding) for tokens 2c and 2c + 1.
+
+// Q operand of a row: entry [i][l] holds dims 32i + 8c .. 32i + 8c + 7 of
+// head l/4 for l/4 < 3 (c = l%4), zeros for the padding rows.
+struct QFrag {
+  uint4 v[8][32];
+};
+
+// Every thread of the CTA calls this (nthreads of them); the caller
+// synchronises before the fragments are read.
+__device__ __forceinline__ void stage_query(const AttentionParams& p, int r, QFrag& qf, int tid,
+                                            int nthreads) {
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q + (int64_t)r * kAttHeads * kAttDim);
+  for (int e = tid; e < 8 * 32; e += nthreads) {
+    const int i = e >> 5, l = e & 31, g = l >> 2, c = l & 3;
+    qf.v[i][l] = g < kAttHeads ? qp[g * (kAttDim / 8) + 4 * i + c] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// A fragment read from shared memory that the compiler may not hoist out of
+// the token loop (it would hold 32 more registers per thread).
+__device__ __forceinline__ uint4 lds_frag(const uint4* a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"((uint32_t)__cvta_generic_to_shared(a)));
+  return v;
+}
+
+// d += A x B for one 16 x 8 x 16 slice; A rows 8..15 are zero
+__device__ __forceinline__ void mma_slice(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// Batch b0's operands (tokens tok[b0 .. b0+8) of tok[0..n)): kr = this
+// lane's 128 bytes of token b0 + l/4's K (the MMA operand), vr = dims
+// [8l, 8l+8) of every token's V (this lane's share of the P.V
+// accumulators); zeros past n.
+__device__ __forceinline__ void mma_load(const AttentionParams& p, const uint32_t* tok, int n,
+                                         int b0, uint4 (&kr)[8], uint4 (&vr)[kBatch], int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  const bool kl = b0 + g < n;
+  const __half* kp = p.kv + (int64_t)tok[kl ? b0 + g : b0] * kKvTokenHalves + 8 * c;
 #pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      if (b0 + t < n) {
-        const __half* tp = p.kv + (int64_t)tok[b0 + t] * kKvTokenHalves;
-        kr[t] = ld_stream16(tp + 8 * lane);
-        vr[t] = ld_stream16(tp + kAttDim + 8 * lane);
-      } else {
-        kr[t] = make_uint4(0, 0, 0, 0);
-        vr[t] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    // partial logits over this lane's 8 dims: x[4t + h]
-    float x[32];
+  for (int i = 0; i < 8; ++i) kr[i] = kl ? ld_stream16(kp + 32 * i) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      const uint32_t w[4] = {kr[t].x, kr[t].y, kr[t].z, kr[t].w};
+  for (int t = 0; t < kBatch; ++t)
+    vr[t] = b0 + t < n
+                ? ld_stream16(p.kv + (int64_t)tok[b0 + t] * kKvTokenHalves + kAttDim + 8 * lane)
+                : make_uint4(0, 0, 0, 0);
+}
+
+// Logits, online softmax and P.V of batch b0 (operands from mma_load).
+__device__ __forceinline__ void mma_batch(const AttentionParams& p, int n, int b0,
+                                          const uint4 (&kr)[8], const uint4 (&vr)[kBatch],
+                                          const QFrag& qf, WarpState& st, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  // two accumulator chains (even / odd i), summed at the end
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int h = 0; h < kAttHeads; ++h) {
-        float a = 0.f;
+  for (int i = 0; i < 8; ++i) {
+    const uint4 q = lds_frag(&qf.v[i][lane]);   // re-read per batch: no registers held
+    float(&d)[4] = (i & 1) ? d1 : d0;
+    mma_slice(d, q.x, q.y, kr[i].x, kr[i].y);
+    mma_slice(d, q.z, q.w, kr[i].z, kr[i].w);
+  }
+  const bool hv = g < kAttHeads;
+  const float z0 = hv && b0 + 2 * c < n ? (d0[0] + d1[0]) * p.scale_log2 : -CUDART_INF_F;
+  const float z1 = hv && b0 + 2 * c + 1 < n ? (d0[1] + d1[1]) * p.scale_log2 : -CUDART_INF_F;
+  // batch max and sum per head over the four lanes of the head
+  float mb = fmaxf(z0, z1);
+  mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+  mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+  const float m_new = fmaxf(st.m_run, mb);
+  const bool any = m_new != -CUDART_INF_F;
+  const float cs = any ? exp2f(st.m_run - m_new) : 1.f;
+  const float p0 = any ? exp2f(z0 - m_new) : 0.f;
+  const float p1 = any ? exp2f(z1 - m_new) : 0.f;
+  float ps = p0 + p1;
+  ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+  st.l_run = fmaf(st.l_run, cs, ps);
+  st.m_run = m_new;
+  // P.V: weight (head h, token t) is in lane 4h + t/2 (p0 for even t)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          a = fma_h(qh[h][m], w[m], false, a);
-          a = fma_h(qh[h][m], w[m], true, a);
-        }
-        x[4 * t + h] = a;
-      }
-      x[4 * t + 3] = 0.f;
-    }
-    const float dot = reduce_scatter32(x, lane);
-    const int tt = lane >> 2;
-    const bool live = hh < kAttHeads && b0 + tt < n;
-    const float z = live ? dot * p.scale_log2 : -CUDART_INF_F;
-    // batch max per head over the 8 tokens (lanes with the same l%4)
-    float mb = z;
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-    const float m_new = fmaxf(st.m_run, mb);
-    const bool any = m_new != -CUDART_INF_F;
-    const float c = any ? exp2f(st.m_run - m_new) : 1.f;
-    const float pz = any ? exp2f(z - m_new) : 0.f;
-    float ps = pz;
-    ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-    st.l_run = fmaf(st.l_run, c, ps);
-    st.m_run = m_new;
-    // P.V over the batch: every lane needs all 24 weights and 3 scales
-    float ch[kAttHeads];
+  for (int h = 0; h < kAttHeads; ++h) {
+    const float ch = __shfl_sync(0xffffffffu, cs, 4 * h);
 #pragma unroll
-    for (int h = 0; h < kAttHeads; ++h) ch[h] = __shfl_sync(0xffffffffu, c, h);
+    for (int d = 0; d < 8; ++d) st.acc[h][d] *= ch;
+  }
 #pragma unroll
-    for (int h = 0; h < kAttHeads; ++h)
+  for (int t = 0; t < kBatch; ++t) {
+    const float2 v01 = h2f2(vr[t].x), v23 = h2f2(vr[t].y), v45 = h2f2(vr[t].z),
+                 v67 = h2f2(vr[t].w);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) st.acc[h][d] *= ch[h];
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      float vf[8];
-      to_f32x8(vr[t], vf);
-#pragma unroll
-      for (int h = 0; h < kAttHeads; ++h) {
-        const float pw = __shfl_sync(0xffffffffu, pz, 4 * t + h);
-#pragma unroll
-        for (int d = 0; d < 8; ++d) st.acc[h][d] = fmaf(pw, vf[d], st.acc[h][d]);
-      }
+    for (int h = 0; h < kAttHeads; ++h) {
+      const float pw = __shfl_sync(0xffffffffu, (t & 1) ? p1 : p0, 4 * h + (t >> 1));
+      const float2 pp = make_float2(pw, pw);
+      float2 a;
+      a = ffma2(pp, v01, make_float2(st.acc[h][0], st.acc[h][1]));
+      st.acc[h][0] = a.x; st.acc[h][1] = a.y;
+      a = ffma2(pp, v23, make_float2(st.acc[h][2], st.acc[h][3]));
+      st.acc[h][2] = a.x; st.acc[h][3] = a.y;
+      a = ffma2(pp, v45, make_float2(st.acc[h][4], st.acc[h][5]));
+      st.acc[h][4] = a.x; st.acc[h][5] = a.y;
+      a = ffma2(pp, v67, make_float2(st.acc[h][6], st.acc[h][7]));
+      st.acc[h][6] = a.x; st.acc[h][7] = a.y;
     }
   }
+}
+
+// The warp's walk over tok[0..n), 8 tokens at a time.  While it runs,
+// lanes 4g..4g+3 keep head g's running (m, l) (g < 3); the state may be
+// carried over several walks, and finish_mma_state() moves it to the
+// WarpState layout for the merge.
+__device__ __forceinline__ void attend_tokens_mma(const AttentionParams& p, const uint32_t* tok,
+                                                  int n, const QFrag& qf, WarpState& st,
+                                                  int lane) {
+  for (int b0 = 0; b0 < n; b0 += kBatch) {
+    uint4 kr[8], vr[kBatch];
+    mma_load(p, tok, n, b0, kr, vr, lane);
+    mma_batch(p, n, b0, kr, vr, qf, st, lane);
+  }
+}
+
+// Keeps the compiler from sinking a batch's arithmetic below the loads of
+// the batches after it (which would hold a third operand set in registers):
+// the state must be final here, before any later volatile load is issued.
+__device__ __forceinline__ void pin_state(WarpState& st) {
+  asm volatile("" : "+f"(st.acc[0][0]), "+f"(st.acc[0][1]), "+f"(st.acc[0][2]),
+               "+f"(st.acc[0][3]), "+f"(st.acc[0][4]), "+f"(st.acc[0][5]), "+f"(st.acc[0][6]),
+               "+f"(st.acc[0][7]), "+f"(st.m_run), "+f"(st.l_run));
+  asm volatile("" : "+f"(st.acc[1][0]), "+f"(st.acc[1][1]), "+f"(st.acc[1][2]),
+               "+f"(st.acc[1][3]), "+f"(st.acc[1][4]), "+f"(st.acc[1][5]), "+f"(st.acc[1][6]),
+               "+f"(st.acc[1][7]));
+  asm volatile("" : "+f"(st.acc[2][0]), "+f"(st.acc[2][1]), "+f"(st.acc[2][2]),
+               "+f"(st.acc[2][3]), "+f"(st.acc[2][4]), "+f"(st.acc[2][5]), "+f"(st.acc[2][6]),
+               "+f"(st.acc[2][7]));
+}
+
+// attend_tokens_mma with the next batch's loads issued before the current
+// batch is computed (two operand sets in registers): a warp always has a
+// batch of K/V in flight.
+__device__ __forceinline__ void attend_tokens_mma_pipe(const AttentionParams& p,
+                                                       const uint32_t* tok, int n,
+                                                       const QFrag& qf, WarpState& st, int lane) {
+  if (n <= 0) return;
+  uint4 ka[8], va[kBatch], kb[8], vb[kBatch];
+  mma_load(p, tok, n, 0, ka, va, lane);
+  for (int b0 = 0; b0 < n; b0 += 2 * kBatch) {
+    if (b0 + kBatch < n) mma_load(p, tok, n, b0 + kBatch, kb, vb, lane);
+    mma_batch(p, n, b0, ka, va, qf, st, lane);
+    pin_state(st);
+    if (b0 + kBatch >= n) break;
+    if (b0 + 2 * kBatch < n) mma_load(p, tok, n, b0 + 2 * kBatch, ka, va, lane);
+    mma_batch(p, n, b0 + kBatch, kb, vb, qf, st, lane);
+    pin_state(st);
+  }
+}
+
+// head h's (m, l) from lane 4h to lane h
+__device__ __forceinline__ void finish_mma_state(WarpState& st, int lane) {
+  const int src = lane < kAttHeads ? 4 * lane : 0;
+  st.m_run = __shfl_sync(0xffffffffu, st.m_run, src);
+  st.l_run = __shfl_sync(0xffffffffu, st.l_run, src);
 }
 
 // Shared memory of a CTA merge: per warp m[3], l[3], acc[3][256].

@@ -95,8 +95,8 @@ def test_attention_config4_full_size_sampled_rows():
 
 @pytest.mark.parametrize("R", [16, 17, 40])
 def test_attention_batch_sizes_around_the_split_switch(R):
-    # batches of up to 16 rows take 64-entry splits, larger ones 256-entry
-    # splits: premade lists with holes and duplicates, every width, bad ids
+    # batches of up to 16 rows take 64-entry splits, larger ones the stream
+    # split: premade lists with holes and duplicates, every width, bad ids
     w = _lists(R, [0, 1, 32, 1024, 2051, 1500, 77], 3000, seed=60 + R)
     pt = w.kv_page_table.clone()
     pt[1, 0] = -1                                   # an unmapped K/V page
@@ -105,6 +105,24 @@ def test_attention_batch_sizes_around_the_split_switch(R):
     got, gerr, oerr, _ = _check(w, w.indices, pt=pt, t2r=t2r)
     assert gerr == oerr
     assert (got[R - 1] == 0).all()
+
+
+@pytest.mark.parametrize("R,L,width", [(17, 3000, 0), (17, 3000, 1), (40, 3000, 33),
+                                        (97, 3000, 300), (300, 2100, 2051), (1100, 700, 2051),
+                                        (1100, 700, 77)])
+def test_attention_stream_runs_across_rows(R, L, width):
+    # batches of more than 16 rows: the index lists cut into 32-entry chunks
+    # laid end to end and split into equal runs, one per CTA of one wave; a
+    # run spans two rows (or three at 1100 rows), a row several runs
+    valid = [min(v, L) for v in (2051, 1500, 77, 0, 32, 513)]
+    w = _lists(R, valid, L, seed=70 + R + width)
+    idx = w.indices[:, :width].contiguous()
+    rows = sorted({0, 1, R // 3, R // 2, R - 2, R - 1})
+    got, gerr, oerr, _ = _check(w, idx, rows=rows)
+    assert gerr == oerr == 0
+    assert np.isfinite(got).all()
+    if width == 0:
+        assert (got == 0).all()
 
 
 def test_attention_single_index_exact():
