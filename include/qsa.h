@@ -221,9 +221,11 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  *
  * Results: out_indices is bit-identical to qsa_select_paged_tokens on the
  * same inputs; out is the attention of qsa_sparse_attention over those
- * indices (FP32 accumulation; the index list is split into runs of 512
- * entries instead of 256, so the last bits of out may differ from the
- * two-call path, within the same bound against the exact result).
+ * indices (FP32 accumulation; the index list is cut into runs and the
+ * logits summed differently from the two-call path -- 512-entry runs and
+ * CUDA-core dot products here, equal runs of the whole batch and
+ * tensor-core chains there -- so the last bits of out may differ, within
+ * the same bound against the exact result).
  *
  * Arguments: the selection's, as qsa_select_paged_tokens (num_reqs rows in
  * both page tables), then the attention's, as qsa_sparse_attention without

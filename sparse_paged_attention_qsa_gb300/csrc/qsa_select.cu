@@ -1179,7 +1179,6 @@ constexpr int kFusedMinRows = 16;   // batches of at most this many rows take th
 
 struct FollowAttnSmem {
   attn::MergeSmem<kFollowWarps> merge;
-  attn::QFrag qf;
   uint32_t tok[kFollowWarps][32];
   attn::CombineSmem<kFusedSplits> comb;
 };
@@ -1279,14 +1278,13 @@ follow_kernel(const SelectParams sp, const AttentionParams ap) {
       if (go) {
         const int req = ap.t2r[r];
         const bool rok = req >= 0 && req < ap.num_reqs;
-        attn::stage_query(ap, r, ash.qf, tid, kFollowThreads);
+        uint32_t qh[kAttHeads][4];
+        attn::load_query(ap, r, lane, qh);
         const int nvalid = attn::resolve_entries<32>(
             ap, r, req, rok, (int64_t)split * kFusedSplit + warp * 32, ash.tok[warp], lane);
-        __syncthreads();                                  // the query fragments are staged
         attn::WarpState st;
         attn::init_state(st);
-        attn::attend_tokens_mma(ap, ash.tok[warp], nvalid, ash.qf, st, lane);
-        attn::finish_mma_state(st, lane);
+        attn::attend_tokens(ap, ash.tok[warp], nvalid, qh, st, lane);
         attn::merge_warps<kFollowWarps>(st, ash.merge, rpart + split * attn::kPartFloats, tid,
                                         warp, lane);
       }
