@@ -216,16 +216,11 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * qsa_select_attend -- one decode step: qsa_select_paged_tokens followed by
  * qsa_sparse_attention over the indices it selects ("vLLM: integrate FP16
  * packed QSA extension", Summary: the fused selection and the exact-packed
- * attention kernel; "Exact contracts" / Selection and Attention), with the
- * attention of early rows running while later rows are still being scored.
+ * attention kernel; "Exact contracts" / Selection and Attention), in one
+ * call with one workspace.
  *
- * Results: out_indices is bit-identical to qsa_select_paged_tokens on the
- * same inputs; out is the attention of qsa_sparse_attention over those
- * indices (FP32 accumulation; the index list is cut into runs and the
- * logits summed differently from the two-call path -- 512-entry runs and
- * CUDA-core dot products here, equal runs of the whole batch and
- * tensor-core chains there -- so the last bits of out may differ, within
- * the same bound against the exact result).
+ * Results: identical to the two calls on the same inputs -- out_indices bit
+ * for bit, out as qsa_sparse_attention over out_indices.
  *
  * Arguments: the selection's, as qsa_select_paged_tokens (num_reqs rows in
  * both page tables), then the attention's, as qsa_sparse_attention without
@@ -234,16 +229,12 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * num_rows, cmp_pt_cols) bytes, 256-byte aligned.  out_indices and out must
  * not overlap each other, any input or the workspace.
  *
- * How it runs: a memset of the workspace's counters, then two kernels on
- * the stream: the score kernel on most SMs, and a follower kernel
- * (launched as its programmatic dependent) on the others, which takes each
- * row's top-k once the row's keys are scored and then the row's attention.
- * A batch of at most 16 rows has little scoring to overlap and runs the
- * kernels of the two separate calls instead (same results).
- * The follower waits on counters the score kernel publishes; every wait
- * gives up after 1 s (QSA_DERR_TIMEOUT in *error_word; the outputs are then
- * incomplete), so a fault can never hang the GPU.  Calls that share a
- * workspace must not overlap on the GPU.
+ * How it runs: the kernels of the two calls on the stream, chained by
+ * programmatic dependent launch (score, top-k, attention, merge); nothing
+ * waits on the host.  (Running the attention of early rows beside the
+ * scoring of later ones was slower at every batch size measured, 17 to 256
+ * rows: the scoring needs every SM to reach the HBM rate.)  Calls that
+ * share a workspace must not overlap on the GPU.
  */
 QSA_API qsa_status qsa_select_attend(
     const void* q_sel, qsa_dtype q_sel_dtype, int64_t num_rows,

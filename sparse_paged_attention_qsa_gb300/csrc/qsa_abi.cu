@@ -190,25 +190,17 @@ qsa_status check_attention(
   return QSA_OK;
 }
 
-// Workspace of the fused call: the selection's score keys for every row, then
-// the attention partials and the counters of one launch (at most
-// kFusedMaxRows rows; longer batches run in chunks that reuse them).
-struct FusedLayout {
-  size_t part, sync, total;
+// Workspace of the one-call step: the selection's score keys and unit
+// maxima, then the attention's partials.
+struct OneCallLayout {
+  size_t part, total;
 };
 
-FusedLayout fused_layout(int64_t num_rows, int64_t cmp_pt_cols) {
-  const int64_t rows = num_rows < qsa::kFusedMaxRows ? num_rows : qsa::kFusedMaxRows;
+OneCallLayout one_call_layout(int64_t num_rows, int64_t cmp_pt_cols) {
   const auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
-  FusedLayout l;
+  OneCallLayout l;
   l.part = up(qsa::select_workspace_bytes(num_rows, cmp_pt_cols));
-  // partials of the follower's 512-entry items, or of the split attention
-  // kernels when a small batch takes the two-kernel route
-  const int64_t splits = std::max<int64_t>(qsa::kFusedSplits,
-                                           qsa::attention_splits(rows, qsa::kOutWidth));
-  l.sync = l.part + up((size_t)rows * splits *
-                       (qsa::kAttHeads * 2 + qsa::kAttHeads * kAttDim) * sizeof(float));
-  l.total = l.sync + up(qsa::fused_sync_bytes(rows));
+  l.total = l.part + up(qsa::attention_workspace_bytes(num_rows, qsa::kOutWidth));
   return l;
 }
 
@@ -243,7 +235,7 @@ size_t qsa_select_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols) {
 
 size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols) {
   if (num_rows <= 0 || cmp_pt_cols <= 0) return 0;
-  return fused_layout(num_rows, cmp_pt_cols).total;
+  return one_call_layout(num_rows, cmp_pt_cols).total;
 }
 
 size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width) {
@@ -362,7 +354,7 @@ qsa_status qsa_select_attend(
                        out_dtype, out_width, out_stride0, scale, out, out_attn_dtype, out_strides,
                        error_word, &a, &o_att, ins_att, &empty_att);
   if (st != QSA_OK || empty) return st;
-  const FusedLayout l = fused_layout(num_rows, cmp_pt_cols);
+  const OneCallLayout l = one_call_layout(num_rows, cmp_pt_cols);
   if (!workspace || workspace_bytes < l.total) return QSA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return QSA_ERR_ALIGN;
   const Span ws = span(workspace, (int64_t)l.total);
@@ -385,9 +377,7 @@ qsa_status qsa_select_attend(
   unsigned char* w = static_cast<unsigned char*>(workspace);
   p.scores = reinterpret_cast<uint32_t*>(w);
   p.umax = p.scores + num_rows * p.vcap;
-  p.sync = reinterpret_cast<uint32_t*>(w + l.sync);
   a.part = reinterpret_cast<float*>(w + l.part);
-  a.nsplit = qsa::kFusedSplits;
   const cudaError_t e = qsa::launch_select_attend(p, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

@@ -1,6 +1,6 @@
-// qsa_attn_impl.cuh -- device code of the sparse attention shared by the
-// attention kernels (qsa_attention.cu) and the fused select -> attend path
-// (qsa_select.cu).
+// qsa_attn_impl.cuh -- device code of the sparse attention kernels
+// (qsa_attention.cu): resolving index lists, the warp's walk over tokens,
+// and the log-sum-exp merges.
 //
 // "vLLM: integrate FP16 packed QSA extension", Summary (exact-packed
 // attention kernel) and "Exact contracts"/Attention: three FP16 query heads
@@ -81,144 +81,6 @@ __device__ __forceinline__ int resolve_entries(const AttentionParams& p, int r, 
   }
   __syncwarp();
   return nvalid;
-}
-
-// --- CUDA-core logits ----------------------------------------------------------
-//
-// The one-call path's follower runs the attention in 16-warp CTAs that hold
-// at most 128 registers per thread; there the tensor-core walk below spills
-// and was slower (0.532 vs 0.518 ms per 256 x 131072 step), so the follower
-// keeps this walk: the logits as 24 fp16-operand dot products per lane and
-// one warp reduce-scatter per batch.
-
-// acc + a*b with fp16 operands and a binary32 accumulator
-__device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, bool hi, float c) {
-  float d;
-  if (hi)
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
-        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  else
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
-        : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-
-__device__ __forceinline__ void to_f32x8(const uint4 v, float* f) {
-  const float2 a = h2f2(v.x), b = h2f2(v.y), c = h2f2(v.z), d = h2f2(v.w);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-}
-
-// Sum 32 per-lane values over the warp, reduce-scatter style: on return
-// x[0] of lane l holds the warp-wide sum of value l (31 shuffles).
-__device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane) {
-#pragma unroll
-  for (int level = 0; level < 5; ++level) {
-    const int half = 16 >> level;            // values kept after this level
-    const int bit = 16 >> level;             // partner lane distance
-    const bool upper = (lane & bit) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? x[i] : x[i + half];
-      const float keep = upper ? x[i + half] : x[i];
-      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-    }
-  }
-  return x[0];
-}
-
-// query dims [8*lane, 8*lane+8) of each head of row r, fp16 pairs
-__device__ __forceinline__ void load_query(const AttentionParams& p, int r, int lane,
-                                           uint32_t (&qh)[kAttHeads][4]) {
-  const uint4* qp = reinterpret_cast<const uint4*>(p.q + (int64_t)r * kAttHeads * kAttDim);
-#pragma unroll
-  for (int h = 0; h < kAttHeads; ++h) {
-    const uint4 v = qp[h * 32 + lane];
-    qh[h][0] = v.x; qh[h][1] = v.y; qh[h][2] = v.z; qh[h][3] = v.w;
-  }
-}
-
-// Walk tokens tok[0..n) kBatch at a time: lane l owns dims [8l, 8l+8) of K
-// and V, so a token's 1 KiB (K then V) is two coalesced 512-byte warp loads
-// and a batch keeps 8 KiB in flight.  The 24 head logits of a batch are
-// reduced with one reduce-scatter, after which lane l holds token l/4, head
-// l%4 (head 3 is padding); the online softmax runs in base 2 with one exp2
-// per lane per batch.
-__device__ __forceinline__ void attend_tokens(const AttentionParams& p, const uint32_t* tok, int n,
-                                              const uint32_t (&qh)[kAttHeads][4], WarpState& st,
-                                              int lane) {
-  const int hh = lane & 3;         // head of this lane's logit after the reduce
-  for (int b0 = 0; b0 < n; b0 += kBatch) {
-    uint4 kr[kBatch], vr[kBatch];
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      if (b0 + t < n) {
-        const __half* tp = p.kv + (int64_t)tok[b0 + t] * kKvTokenHalves;
-        kr[t] = ld_stream16(tp + 8 * lane);
-        vr[t] = ld_stream16(tp + kAttDim + 8 * lane);
-      } else {
-        kr[t] = make_uint4(0, 0, 0, 0);
-        vr[t] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    // partial logits over this lane's 8 dims: x[4t + h]
-    float x[32];
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      const uint32_t w[4] = {kr[t].x, kr[t].y, kr[t].z, kr[t].w};
-#pragma unroll
-      for (int h = 0; h < kAttHeads; ++h) {
-        float a = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          a = fma_h(qh[h][m], w[m], false, a);
-          a = fma_h(qh[h][m], w[m], true, a);
-        }
-        x[4 * t + h] = a;
-      }
-      x[4 * t + 3] = 0.f;
-    }
-    const float dot = reduce_scatter32(x, lane);
-    const int tt = lane >> 2;
-    const bool live = hh < kAttHeads && b0 + tt < n;
-    const float z = live ? dot * p.scale_log2 : -CUDART_INF_F;
-    // batch max per head over the 8 tokens (lanes with the same l%4)
-    float mb = z;
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-    const float m_new = fmaxf(st.m_run, mb);
-    const bool any = m_new != -CUDART_INF_F;
-    const float c = any ? exp2f(st.m_run - m_new) : 1.f;
-    const float pz = any ? exp2f(z - m_new) : 0.f;
-    float ps = pz;
-    ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-    st.l_run = fmaf(st.l_run, c, ps);
-    st.m_run = m_new;
-    // P.V over the batch: every lane needs all 24 weights and 3 scales
-    float ch[kAttHeads];
-#pragma unroll
-    for (int h = 0; h < kAttHeads; ++h) ch[h] = __shfl_sync(0xffffffffu, c, h);
-#pragma unroll
-    for (int h = 0; h < kAttHeads; ++h)
-#pragma unroll
-      for (int d = 0; d < 8; ++d) st.acc[h][d] *= ch[h];
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      float vf[8];
-      to_f32x8(vr[t], vf);
-#pragma unroll
-      for (int h = 0; h < kAttHeads; ++h) {
-        const float pw = __shfl_sync(0xffffffffu, pz, 4 * t + h);
-#pragma unroll
-        for (int d = 0; d < 8; ++d) st.acc[h][d] = fmaf(pw, vf[d], st.acc[h][d]);
-      }
-    }
-  }
 }
 
 // --- tensor-core logits --------------------------------------------------------

@@ -48,21 +48,9 @@ struct SelectParams {
   uint32_t* umax;             // workspace: [R, vcap/16] largest key of each run of 16 blocks
   int64_t vcap;               // pt_cols * 128
   uint32_t* err;              // nullable
-  uint32_t* sync;             // fused select -> attend only: counters (kSync*), else null
   int R;
 };
 
-// Counters of the fused select -> attend path, zeroed before each launch
-// (32-bit words): items claimed by the follower kernel, a follower wait that
-// gave up, then per row: pages scored and published, top-k state (1 done,
-// 2 failed), attention items done.
-constexpr int kSyncItem = 1;
-constexpr int kSyncAbort = 2;
-constexpr int kSyncRows = 4;
-constexpr int kFusedSplit = 512;                                   // entries per attention item
-constexpr int kFusedSplits = (kOutWidth + kFusedSplit - 1) / kFusedSplit;   // 5
-constexpr int kFusedMaxRows = 1024;                                // rows per fused launch
-inline size_t fused_sync_bytes(int64_t R) { return (size_t)(kSyncRows + 3 * R) * 4; }
 
 struct AttentionParams {
   const __half* q;            // [R,3,256]
@@ -105,9 +93,8 @@ size_t select_workspace_bytes(int64_t R, int64_t pt_cols);
 size_t attention_workspace_bytes(int64_t R, int64_t width);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream);
-// Fused select -> attend: a.idx must be p.out (the selection's output), a.part
-// a partial buffer of min(R, kFusedMaxRows) * kFusedSplits partials, p.sync
-// fused_sync_bytes(min(R, kFusedMaxRows)) bytes.
+// Select, then attend over the selection's output (a.idx, a.width and
+// a.nsplit are set here); a.part holds attention_workspace_bytes(R, 2051).
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream);
 int attention_splits(int64_t R, int64_t width);

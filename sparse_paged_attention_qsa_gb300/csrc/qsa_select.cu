@@ -27,7 +27,6 @@
 // so float order equals unsigned order); 0 marks a block without a key.
 #include "qsa_internal.h"
 #include "qsa_device.cuh"
-#include "qsa_attn_impl.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -54,8 +53,6 @@ constexpr int kScoreThreads = (kScoreWarps + 1) * 32;   // + one producer warp
 constexpr int kKeyGroups = kCmpPageKeys / 8;            // groups of 8 keys per page
 static_assert(2 * kScoreWarps == kKeyGroups, "each consumer warp takes whole key-group pairs");
 constexpr int kMaxRows = 1024;                          // rows per launch (row tables in smem)
-static_assert(kMaxRows == kFusedMaxRows, "one row chunk per fused launch");
-constexpr int kChunkPages = 32;  // fused path: pages of a group per unit (1 MiB of fp16 keys)
 // The score kernel also keeps the largest key of each run of 16 blocks (one
 // warp step: two groups of 8 keys), so the top-k reads 1/16 of a row first.
 constexpr int kUnitKeys = 16;
@@ -135,20 +132,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
-}
-// Release-ordered atomic add at GPU scope: everything this thread wrote or
-// observed before (the consumer warps' keys, seen through the stage's
-// mbarrier) is visible to a thread that acquires the new value.
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t mbar, uint64_t policy) {
@@ -289,11 +272,6 @@ __device__ __forceinline__ void load_key_groups(uint32_t stage, int g0, int t, i
   }
 }
 
-struct StageRec {
-  int g;          // group of the unit whose last loaded page is in the stage (-1: none)
-  int c0, c1;     // the unit's page-table columns [c0, c1)
-};
-
 struct StageDesc {
   int row;        // first row of the group; -1: no more work
   int b0;         // first block of the page
@@ -337,7 +315,7 @@ __device__ __forceinline__ int page_cost(int n) {
 // 2k + t/2, 16-byte chunks (4(t&1)+j) XOR (row & 7): the 8 lanes of each
 // shared-memory phase hit 8 distinct bank groups, and each lane reads its
 // slice in ascending order.
-template <bool kFp8, bool kFused>
+template <bool kFp8>
 __global__ void __launch_bounds__(kScoreThreads, 1)
 score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   constexpr int kPageBytes = KeyCfg<kFp8>::kPageBytes;
@@ -347,7 +325,6 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   __shared__ int64_t s_total;
   __shared__ int s_ngroups;
   __shared__ int64_t warp_sum[kScoreWarps];
-  __shared__ StageRec rec[kMaxStages];   // fused path: the page in each stage
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   const uint32_t base = raw + pad;
@@ -445,8 +422,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
         for (int r = f; r < l; ++r) vmax = row_vs[r] > vmax ? row_vs[r] : vmax;
         const int pages = (vmax + kCmpPageKeys - 1) / kCmpPageKeys;
         grp_pages[gi] = pages;
-        wg[i] = kFused ? (int64_t)((pages + kChunkPages - 1) / kChunkPages)   // chunks
-                       : (int64_t)pages * page_cost<kFp8>(l - f);
+        wg[i] = (int64_t)pages * page_cost<kFp8>(l - f);
       }
       wsum += wg[i];
     }
@@ -472,121 +448,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   volatile int* abort_flag = &s_abort;
   int64_t issued = 0;
 
-  if (kFused && is_producer_warp) {
-    // ------------- producer of the fused path (one lane) -------------
-    // Units of kChunkPages pages of a group, interleaved over the CTAs (CTA
-    // b takes units b, b + grid, ...), so rows finish in row order while
-    // the follower kernel picks them up.  A unit is published (row_done +=
-    // its pages each row of the group sees) once the stage of its last
-    // loaded page is released by every consumer warp (they consume stages
-    // in order), or at once if none of its pages could be loaded.
-    if (lane == 0) {
-      const uint64_t policy = evict_first_policy();
-      const int NG = s_ngroups;
-      uint32_t* const row_done = p.sync + kSyncRows;
-      const auto publish = [&](int g, int c0, int c1) {
-        const int f = grp_first[g], l = grp_first[g + 1];
-        for (int r = f; r < l; ++r) {
-          const int pr = (row_vs[r] + kCmpPageKeys - 1) / kCmpPageKeys;   // pages row r sees
-          const int add = min(c1, pr) - c0;
-          if (add > 0) red_release_add(row_done + r, (uint32_t)add);
-        }
-      };
-      for (int i = 0; i < kStages; ++i) rec[i].g = -1;
-      int pgrp = 0, pcol = 0, pend = 0, c0 = 0;   // current unit: group, next page, end, first
-      int last_s = -1;                             // stage of the unit's latest loaded page
-      int64_t next_u = blockIdx.x;
-      for (;;) {
-        const int s = (int)(issued % kStages);
-        const uint32_t ph = (uint32_t)((issued / kStages) & 1);
-        if (issued >= kStages) {
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
-            *abort_flag = 1;
-            report(p.err, kErrTimeout);
-            break;
-          }
-          if (rec[s].g >= 0) {
-            publish(rec[s].g, rec[s].c0, rec[s].c1);
-            rec[s].g = -1;
-          }
-        }
-        if (*abort_flag) break;
-        bool done = false;
-        for (;;) {   // next page with a loadable physical page
-          if (pcol >= pend) {
-            if (pend > 0) {          // the unit in progress is complete
-              if (last_s >= 0) {
-                rec[last_s].g = pgrp;
-                rec[last_s].c0 = c0;
-                rec[last_s].c1 = pend;
-              } else {
-                publish(pgrp, c0, pend);
-              }
-            }
-            const int64_t u = next_u;
-            next_u += gridDim.x;
-            if (u >= W || NG == 0) {
-              done = true;
-              break;
-            }
-            int lo = 0, hi = NG - 1;          // last group with grp_pre <= u
-            while (lo < hi) {
-              const int mid = (lo + hi + 1) >> 1;
-              if (grp_pre[mid] <= u) lo = mid; else hi = mid - 1;
-            }
-            pgrp = lo;
-            c0 = pcol = (int)(u - grp_pre[lo]) * kChunkPages;
-            pend = min(pcol + kChunkPages, grp_pages[lo]);
-            last_s = -1;
-          }
-          const int row0 = grp_first[pgrp];
-          const int n = grp_first[pgrp + 1] - row0;
-          const int col = pcol++;
-          const int32_t pg = __ldg(p.pt + (int64_t)row_req[row0] * p.pt_stride0 + col);
-          if (pg >= 0 && pg < p.num_pages) {
-            desc[s].row = row0;
-            desc[s].b0 = col * kCmpPageKeys;
-            desc[s].nrows = n;
-            last_s = s;
-            ++issued;
-            mbar_expect_tx(bar_full + 8 * s, kPageBytes);
-            tma_load_2d(base + s * kPageBytes, &tmap, 0,
-                        pg * KeyCfg<kFp8>::kRowsPerKey * kCmpPageKeys, bar_full + 8 * s, policy);
-            break;
-          }
-          for (int j = 0; j < n; ++j) {          // no key for these blocks
-            const int nk = min(row_vs[row0 + j] - col * kCmpPageKeys, kCmpPageKeys);
-            uint32_t* zr = p.scores + (int64_t)(row0 + j) * p.vcap + col * kCmpPageKeys;
-            for (int k = 0; k < nk; ++k) zr[k] = 0u;
-            uint32_t* zu = p.umax + (int64_t)(row0 + j) * (p.vcap / kUnitKeys) +
-                           col * (kCmpPageKeys / kUnitKeys);
-            for (int k = 0; kUnitKeys * k < nk; ++k) zu[k] = 0u;
-          }
-          report(p.err, kErrCmpPage);
-        }
-        if (done) {                 // no more units: mark the stage as the end
-          desc[s].row = -1;
-          ++issued;
-          mbar_arrive(bar_full + 8 * s);
-          break;
-        }
-      }
-      // publish the units whose last page is still in the ring once released
-      if (!*abort_flag) {
-        for (int64_t n = issued > kStages ? issued - kStages : 0; n < issued; ++n) {
-          const int s = (int)(n % kStages);
-          if (rec[s].g < 0) continue;
-          if (!mbar_wait(bar_empty + 8 * s, (uint32_t)((n / kStages) & 1))) {
-            *abort_flag = 1;
-            report(p.err, kErrTimeout);
-            break;
-          }
-          publish(rec[s].g, rec[s].c0, rec[s].c1);
-          rec[s].g = -1;
-        }
-      }
-    }
-  } else if (is_producer_warp) {
+  if (is_producer_warp) {
     // ---------------- producer (one lane) ----------------
     if (lane == 0) {
       const uint64_t policy = evict_first_policy();
@@ -914,18 +776,16 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
   return ((unsigned long long)hi << 32) | lo;
 }
 
-// Top-k of row r by the CTA's kTopkThreads threads into `sh`.  kStandalone:
-// the CTA runs in the top-k kernel, a programmatic dependent of the score
-// kernel, and waits for it after the row's setup; otherwise the caller has
-// already seen the row's keys complete.  Ends after its last write of
+// Top-k of row r by the CTA's kTopkThreads threads into `sh`.  The CTA
+// runs in the top-k kernel, a programmatic dependent of the score kernel,
+// and waits for it after the row's setup.  Ends after its last write of
 // p.out (no final barrier).
-template <bool kStandalone>
 __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31;
   const RowSetup rs = row_setup(p, r);
   int32_t* out = p.out + (int64_t)r * p.out_stride0;
   if (!rs.ok) {
-    if (kStandalone) pdl_wait();
+    pdl_wait();
     for (int j = tid; j < kOutWidth; j += kTopkThreads) out[j] = -1;
     if (tid == 0) report(p.err, kErrRequest);
     return;
@@ -944,7 +804,7 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
     sh.ncand = 0;
   }
   __syncthreads();
-  if (kStandalone) pdl_wait();      // the score kernel's keys are complete and visible
+  pdl_wait();      // the score kernel's keys are complete and visible
 
   // 1. unit maxima: how many are nonzero, the smallest nonzero, the largest
   // (M, the row's largest key); staged in shared memory
@@ -1151,156 +1011,7 @@ topk_kernel(const SelectParams p) {
   extern __shared__ __align__(16) unsigned char topk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   pdl_trigger();   // a dependent (the attention kernel) may be scheduled early (it waits)
-  topk_row<true>(p, blockIdx.x, sh);
-}
-
-// ---------------------------------------------------------------------------
-// fused select -> attend: the follower kernel
-// ---------------------------------------------------------------------------
-//
-// Runs beside the fused score kernel (launched as its programmatic dependent
-// on the SMs the score kernel leaves free; more CTAs start as score CTAs
-// exit).  Its CTAs claim items from a shared counter: each row's top-k, and
-// the row's kFusedSplits attention items of 512 index entries, which trail
-// the top-k items by kItemLag rows so that a row's indices are usually ready
-// when its attention items are claimed.  A top-k item waits until every page
-// of its row is scored and published; an attention item waits for its row's
-// top-k.  The indices go to the caller's output and are read back from L2 by
-// the attention items; the last attention item of a row merges the row's
-// partials into the FP16 output.  Waits are bounded (1 s, then the error
-// word's timeout bit and an abort flag that ends every other wait).
-
-constexpr int kFollowThreads = kTopkThreads;            // 16 warps
-constexpr int kFollowWarps = kFollowThreads / 32;
-static_assert(kFusedSplit == kFollowWarps * 32, "one 32-entry run per warp and item");
-constexpr int kItemLag = 4;
-constexpr int kFollowSMs = 40;                          // SMs the score kernel leaves free
-constexpr int kFusedMinRows = 16;   // batches of at most this many rows take the split kernels
-
-struct FollowAttnSmem {
-  attn::MergeSmem<kFollowWarps> merge;
-  uint32_t tok[kFollowWarps][32];
-  attn::CombineSmem<kFusedSplits> comb;
-};
-constexpr size_t kFollowSmem =
-    sizeof(TopkShared) > sizeof(FollowAttnSmem) ? sizeof(TopkShared) : sizeof(FollowAttnSmem);
-
-// Item i of R rows -> (row, split); split < 0 is the row's top-k.  Order:
-// top-k 0..L-1, then per row k >= L: top-k k and the attention items of row
-// k-L, then the attention items of the last L rows (L = kItemLag).
-__device__ __forceinline__ void decode_item(int i, int R, int& r, int& split) {
-  constexpr int S = kFusedSplits;
-  const int L = R < kItemLag ? R : kItemLag;
-  if (i < L) {
-    r = i;
-    split = -1;
-    return;
-  }
-  const int j = i - L;
-  const int mid = (R - L) * (1 + S);
-  if (j < mid) {
-    const int k = L + j / (1 + S), o = j % (1 + S);
-    if (o == 0) {
-      r = k;
-      split = -1;
-    } else {
-      r = k - L;
-      split = o - 1;
-    }
-    return;
-  }
-  const int j2 = j - mid;
-  r = R - L + j2 / S;
-  split = j2 % S;
-}
-
-// Wait (one thread) until *a >= target.  False if this wait or another one
-// gave up (then nothing is computed from the awaited data).
-__device__ bool wait_at_least(const uint32_t* a, uint32_t target, uint32_t* abort, uint32_t* err) {
-  if (ld_acquire(a) >= target) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    __nanosleep(256);
-    if (ld_acquire(a) >= target) return true;
-    if (*reinterpret_cast<volatile uint32_t*>(abort) != 0u) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      atomicExch(abort, 1u);
-      report(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kFollowThreads, 1)
-follow_kernel(const SelectParams sp, const AttentionParams ap) {
-  extern __shared__ __align__(16) unsigned char follow_smem[];
-  TopkShared& tsh = *reinterpret_cast<TopkShared*>(follow_smem);
-  FollowAttnSmem& ash = *reinterpret_cast<FollowAttnSmem*>(follow_smem);
-  __shared__ int s_item, s_go, s_last;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int R = sp.R;
-  uint32_t* const sync = sp.sync;
-  uint32_t* const row_done = sync + kSyncRows;
-  uint32_t* const topk_done = row_done + R;
-  uint32_t* const attn_done = topk_done + R;
-  const int total = R * (1 + kFusedSplits);
-  for (;;) {
-    if (tid == 0) s_item = (int)atomicAdd(sync + kSyncItem, 1u);
-    __syncthreads();
-    const int i = s_item;
-    if (i >= total) break;
-    int r, split;
-    decode_item(i, R, r, split);
-    if (split < 0) {
-      // ---- top-k of row r once its pages are scored ----
-      if (tid == 0) {
-        const RowSetup rs = row_setup(sp, r);
-        const int64_t Vs = !rs.ok ? 0 : (rs.V < sp.vcap ? rs.V : sp.vcap);
-        const uint32_t pages = (uint32_t)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
-        s_go = wait_at_least(row_done + r, pages, sync + kSyncAbort, sp.err);
-      }
-      __syncthreads();
-      if (s_go) topk_row<false>(sp, r, tsh);
-      __syncthreads();                                    // the row's indices are written
-      if (tid == 0) {
-        __threadfence();
-        st_release(topk_done + r, s_go ? 1u : 2u);
-      }
-    } else {
-      // ---- attention item (r, split) once the row's indices are out ----
-      if (tid == 0) {
-        s_go = wait_at_least(topk_done + r, 1u, sync + kSyncAbort, sp.err) &&
-               ld_acquire(topk_done + r) == 1u;
-      }
-      __syncthreads();
-      const bool go = s_go != 0;
-      float* const rpart = ap.part + (int64_t)r * kFusedSplits * attn::kPartFloats;
-      if (go) {
-        const int req = ap.t2r[r];
-        const bool rok = req >= 0 && req < ap.num_reqs;
-        uint32_t qh[kAttHeads][4];
-        attn::load_query(ap, r, lane, qh);
-        const int nvalid = attn::resolve_entries<32>(
-            ap, r, req, rok, (int64_t)split * kFusedSplit + warp * 32, ash.tok[warp], lane);
-        attn::WarpState st;
-        attn::init_state(st);
-        attn::attend_tokens(ap, ash.tok[warp], nvalid, qh, st, lane);
-        attn::merge_warps<kFollowWarps>(st, ash.merge, rpart + split * attn::kPartFloats, tid,
-                                        warp, lane);
-      }
-      __syncthreads();                                    // this item's partial is written
-      if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(attn_done + r, 1u) == (uint32_t)(kFusedSplits - 1);
-      }
-      __syncthreads();
-      if (s_last && go) {   // every partial of the row is written: merge them
-        __threadfence();
-        attn::combine_row<kFusedSplits>(ap, r, rpart, kFusedSplits, ash.comb, tid);
-      }
-    }
-    __syncthreads();                                      // shared memory and s_item reuse
-  }
+  topk_row(p, blockIdx.x, sh);
 }
 
 }  // namespace
@@ -1366,14 +1077,10 @@ cudaError_t device_info(DeviceInfo** out) {
   if (!d.smem_set) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    for (auto k : {score_kernel<false, false>, score_kernel<true, false>,
-                   score_kernel<false, true>, score_kernel<true, true>}) {
+    for (auto k : {score_kernel<false>, score_kernel<true>}) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
       if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(follow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kFollowSmem);
-    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kTopkSmem);
     if (e != cudaSuccess) return e;
@@ -1406,9 +1113,9 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
     if (c.key_fp8)
-      score_kernel<true, false><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
+      score_kernel<true><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
     else
-      score_kernel<false, false><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
+      score_kernel<false><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
     e = launch_after(topk_kernel, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c);
     if (e != cudaSuccess) return e;
   }
@@ -1417,61 +1124,18 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
 
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream) {
+  // the selection's kernels, then the attention's over its output, all on
+  // the caller's stream; the top-k is a programmatic dependent of the score
+  // kernel, and the attention of batches of up to 16 rows of the top-k
   if (p.R == 0) return cudaSuccess;
-  if (p.R <= kFusedMinRows) {
-    // a small batch has little scoring to overlap: the split kernels (selection,
-    // then attention over its output) finish sooner
-    cudaError_t e = launch_select(p, stream);
-    if (e != cudaSuccess) return e;
-    AttentionParams ac = a;
-    ac.idx = p.out;
-    ac.idx_stride0 = p.out_stride0;
-    ac.width = kOutWidth;
-    ac.nsplit = attention_splits(p.R, kOutWidth);
-    return launch_attention(ac, stream);
-  }
-  DeviceInfo* di = nullptr;
-  cudaError_t e = device_info(&di);
+  cudaError_t e = launch_select(p, stream);
   if (e != cudaSuccess) return e;
-  CUtensorMap map;
-  e = encode_cmp_map(p, &map);
-  if (e != cudaSuccess) return e;
-  // rows in chunks of kMaxRows, one after the other on the stream (the sync
-  // counters and partials are reused)
-  for (int r0 = 0; r0 < p.R; r0 += kMaxRows) {
-    SelectParams c = p;
-    c.R = p.R - r0 < kMaxRows ? p.R - r0 : kMaxRows;
-    c.q_sel = p.q_sel + (int64_t)r0 * kSelHeads * kSelDim;
-    c.t2r = p.t2r + r0;
-    c.qpos = p.qpos + r0;
-    c.out = p.out + (int64_t)r0 * p.out_stride0;
-    c.scores = p.scores + (int64_t)r0 * p.vcap;
-    c.umax = p.umax + (int64_t)r0 * (p.vcap / kUnitKeys);
-    AttentionParams ac = a;
-    ac.R = c.R;
-    ac.q = a.q + (int64_t)r0 * kAttHeads * kAttDim;
-    ac.t2r = c.t2r;
-    ac.idx = c.out;
-    ac.idx_stride0 = p.out_stride0;
-    ac.width = kOutWidth;
-    ac.out = a.out + (int64_t)r0 * kAttHeads * kAttDim;
-    ac.nsplit = kFusedSplits;
-    e = cudaMemsetAsync(c.sync, 0, fused_sync_bytes(c.R), stream);
-    if (e != cudaSuccess) return e;
-    const int64_t items = (int64_t)c.R * c.pt_cols;
-    const int free_sms = di->sms > 2 * kFollowSMs ? di->sms - kFollowSMs : (di->sms + 1) / 2;
-    const int grid = (int)(items < free_sms ? items : free_sms);
-    if (c.key_fp8)
-      score_kernel<true, true><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
-    else
-      score_kernel<false, true><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
-    // the follower starts once every score CTA is running (they trigger at
-    // their start) and never waits for the score grid to finish
-    e = launch_after(follow_kernel, dim3((unsigned)di->sms), dim3(kFollowThreads), kFollowSmem,
-                     stream, c, ac);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
+  AttentionParams ac = a;
+  ac.idx = p.out;
+  ac.idx_stride0 = p.out_stride0;
+  ac.width = kOutWidth;
+  ac.nsplit = attention_splits(p.R, kOutWidth);
+  return launch_attention(ac, stream);
 }
 
 }  // namespace qsa

@@ -5,13 +5,13 @@ indices ("vLLM: integrate FP16 packed QSA extension", Summary and "Exact
 contracts"/Selection and Attention; the pages' tie, tail, saturation and
 multi-request cases).
 
-A batch of more than 16 rows runs a score kernel and a follower kernel
-that waits on per-row counters (the attention of early rows overlaps the
-scoring of later ones); a smaller batch runs the two calls' kernels.  The
-edge cases run both ways (the row list repeated past 16 rows), and the
-tests also cover row chunks (more than 1024 rows), speculative rows that
-share a request, and repeated calls on a dirty workspace.  Tolerance as in
-test_gpu_attention.py.
+The call runs the two calls' kernels from one workspace, so its outputs
+must equal the two calls' bit for bit.  The attention cuts the index lists
+differently on either side of 16 rows (64-entry splits, or equal runs over
+the batch): the edge cases run both ways (the row list repeated past 16
+rows), and the tests also cover row chunks (more than 1024 rows),
+speculative rows that share a request, and repeated calls on a dirty
+workspace.  Tolerance as in test_gpu_attention.py.
 """
 import numpy as np
 import pytest
@@ -75,11 +75,11 @@ def test_fused_matches_two_call_path():
     got_idx, got_out, gerr = _fused(w)
     assert gerr == 0
     assert np.array_equal(got_idx, idx2.cpu().numpy())
-    assert np.abs(got_out - out2.float().cpu().numpy()).max() <= TOL
+    assert np.array_equal(got_out, out2.float().cpu().numpy())     # the same kernels
 
 
 def _rows(lens, big):
-    """The row list, repeated past 16 rows when the follower route is wanted."""
+    """The row list, repeated past 16 rows when the large-batch attention is wanted."""
     return lens * (17 // len(lens) + 1) if big else lens
 
 
