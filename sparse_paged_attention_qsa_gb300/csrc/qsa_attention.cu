@@ -169,9 +169,12 @@ attn_stream_kernel(const AttentionParams p, const StreamPlan sp) {
       if (j0 < c1) n = resolve_piece(p, r, req, rok, j0, c1, sm_tok[warp], lane);
     }
     attn::finish_mma_state(st, lane);
+    // the row's slot; < p.nsplit by the plan's run length (checked on the
+    // host), guarded here so a plan error can never write past the row
     const int64_t slot = b - run_of(r * sp.C, sp);
-    attn::merge_warps<kAttWarps>(st, sm, p.part + (r * p.nsplit + slot) * kPartFloats, tid, warp,
-                                 lane);
+    attn::merge_warps<kAttWarps>(st, sm, p.part + (r * p.nsplit + (slot < p.nsplit ? slot : 0)) *
+                                                      kPartFloats,
+                                 tid, warp, lane);
     __syncthreads();   // shared memory is reused by the next segment
     x = r * sp.C + c1;
   }
@@ -251,6 +254,11 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream) {
     const int64_t lmin = need > kMinRunChunks ? need : kMinRunChunks;
     const int64_t g = sp.T / lmin;
     sp.G = g < 1 ? 1 : (g < slots ? g : slots);
+    // the shortest run, floor(T/G), must keep a row within kStreamSlots runs
+    const int64_t shortest = sp.T / sp.G;
+    if (sp.G > 1 && (sp.C - 1 + shortest - 1) / shortest + 1 > kStreamSlots)
+      return cudaErrorInvalidValue;
+    if (p.nsplit < kStreamSlots) return cudaErrorInvalidValue;
     // a plain launch, not a programmatic dependent of the selection's top-k:
     // the runs are sized for a GPU-wide single wave, and CTAs placed early
     // beside the top-k's made the end-to-end step 0.483 ms instead of 0.444
