@@ -79,7 +79,7 @@ attn_partial_kernel(const AttentionParams p) {
 // to end (T = R*C chunks) and cut into G equal runs, one per CTA, with G the
 // number of CTAs the GPU holds at once: one wave, every CTA streams the same
 // number of entries, and a CTA's dependent index -> page-table -> K/V chain
-// is paid once per row it touches instead of once per 256 entries.  A run
+// is paid once per row it touches instead of once per fixed-width split.  A run
 // crosses row boundaries; per row it touches, the CTA merges its four warps
 // and writes one partial into the row's slot b - b_lo(row), b_lo(row) being
 // the first CTA whose run reaches the row.  Every run holds at least Lmin
