@@ -86,7 +86,7 @@ constexpr int kProdTiles = 4;               // tiles the producer arms per itera
 constexpr size_t kLogitSmem = 220 * 1024;
 constexpr size_t kTablesBytes = (size_t)(kMaxBatch + 1) * 8 + (size_t)kMaxBatch * 4;
 constexpr size_t kMiscBytes = 1024;         // barriers + stage descriptors
-constexpr uint64_t kWaitNs = 1000000000ull;
+
 constexpr uint32_t kErrTimeoutBit = 8u;
 constexpr uint32_t kErrBlockBit = QSA_DERR_IDX_BLOCK;
 
@@ -117,73 +117,8 @@ struct TileDesc {
                      // request's last tile in this CTA (frees the slot)
 };
 
-// --- PTX helpers -------------------------------------------------------------
+// --- PTX helpers (the mbarrier, TMA and bulk-copy ones are in qsa_device.cuh) ---
 
-__device__ __forceinline__ uint64_t gtime() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Test the phase; a thread whose phase is not complete is suspended until it
-// completes or about 20 us pass (the hint), so waiting warps do not take
-// issue slots from the warps doing the work.
-__device__ __forceinline__ bool try_wait(uint32_t a, uint32_t ph, uint32_t hint_ns = 20000u) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(a), "r"(ph), "r"(hint_ns) : "memory");
-  return ok != 0;
-}
-// Non-blocking test of a phase (cheaper than try_wait when it has completed).
-__device__ __forceinline__ bool test_wait(uint32_t a, uint32_t ph) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(a), "r"(ph) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool wait_phase(uint32_t a, uint32_t ph) {
-  if (test_wait(a, ph)) return true;
-  const uint64_t t0 = gtime();
-  while (!try_wait(a, ph))
-    if (gtime() - t0 > kWaitNs) return false;
-  return true;
-}
-__device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ void bar_expect(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x),
-      "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* m, int x, int y,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x),
-      "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // K-major operand, rows of 128 bytes, 128-byte swizzle, 8-row atoms 1024 B apart
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
@@ -313,18 +248,18 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      bar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 1);
       // the tile's MMAs done reading the values (tcgen05.commit) + the four
       // epilogue warps done reading the scales and the descriptor
-      bar_init(bar_empty + 8 * s, 1 + 4);
+      mbar_init(bar_empty + 8 * s, 1 + 4);
     }
     for (int a = 0; a < kMaxAcc; ++a) {
-      bar_init(bar_accf + 8 * a, 1);
-      bar_init(bar_acce + 8 * a, 4);     // the four warps of the group that had the tile
+      mbar_init(bar_accf + 8 * a, 1);
+      mbar_init(bar_acce + 8 * a, 4);     // the four warps of the group that had the tile
     }
     for (int k = 0; k < 2; ++k) {
-      bar_init(bar_qfull + 8 * k, 1);
-      bar_init(bar_qempty + 8 * k, 1 + 4);
+      mbar_init(bar_qfull + 8 * k, 1);
+      mbar_init(bar_qempty + 8 * k, 1 + 4);
     }
     s_abort = 0;
     s_end_tile = INT64_MAX;
@@ -416,7 +351,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       const int stop = __shfl_sync(0xffffffffu, *abort_flag, 0);
       if (stop) break;
       if (w >= w_end) {                 // range done: an end marker in the next stage
-        bool ok = round == 0 || wait_phase(bar_empty + 8 * s, (uint32_t)((round - 1) & 1));
+        bool ok = round == 0 || mbar_wait_sleep(bar_empty + 8 * s, (uint32_t)((round - 1) & 1));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) {
@@ -428,14 +363,14 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) {
           *end_tile = issued;           // the first tile index past the range
           desc[s].b = -1;
-          bar_arrive(bar_full + 8 * s);
+          mbar_arrive(bar_full + 8 * s);
         }
         ++issued;
         break;
       }
       if (b != cur_b) {                 // a new request: its query rows into the next slot
         slot = segs & 1;
-        bool ok = segs < 2 || wait_phase(bar_qempty + 8 * slot, (uint32_t)(((segs >> 1) - 1) & 1));
+        bool ok = segs < 2 || mbar_wait_sleep(bar_qempty + 8 * slot, (uint32_t)(((segs >> 1) - 1) & 1));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) {
@@ -447,9 +382,9 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) {
           const uint32_t qf = bar_qfull + 8 * slot;
           const uint32_t qs = base + qslots + (uint32_t)(slot * p.qslot_bytes);
-          bar_expect(qf, (uint32_t)N * kDim + (uint32_t)N * 4);
-          tma_2d(qs, &qmap, 0, p.qrow0 + b * N, qf);
-          bulk_copy(qs + wOff, p.w + (int64_t)b * N, (uint32_t)N * 4, qf);
+          mbar_expect_tx(qf, (uint32_t)N * kDim + (uint32_t)N * 4);
+          tma_load_2d(qs, &qmap, 0, p.qrow0 + b * N, qf);
+          bulk_load(qs + wOff, p.w + (int64_t)b * N, (uint32_t)N * 4, qf);
         }
         cur_b = b;
         ++segs;
@@ -463,7 +398,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         st -= S;
         ++rd;
       }
-      bool ok = !active || rd == 0 || wait_phase(bar_empty + 8 * st, (uint32_t)((rd - 1) & 1));
+      bool ok = !active || rd == 0 || mbar_wait_sleep(bar_empty + 8 * st, (uint32_t)((rd - 1) & 1));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) {
@@ -498,14 +433,14 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         desc[st].missing = mt;
         desc[st].qinfo = (uint32_t)slot | ((uint32_t)(((segs - 1) >> 1) & 1) << 1) |
                          ((uint32_t)last << 2);
-        bar_expect(full, (uint32_t)__popc(vt) * (uint32_t)p.bs * (kDim + 4));
+        mbar_expect_tx(full, (uint32_t)__popc(vt) * (uint32_t)p.bs * (kDim + 4));
         if (mt) report(p.err, kErrBlockBit);
       }
       __syncwarp();
       if (valid) {
         const uint32_t sb = base + (uint32_t)(st * p.stage_bytes);
-        tma_3d(sb + (uint32_t)(c_lane * p.bs * kDim), &kmap, 0, 0, id, full);
-        bulk_copy(sb + scOff + (uint32_t)(c_lane * p.bs * 4),
+        tma_load_3d(sb + (uint32_t)(c_lane * p.bs * kDim), &kmap, 0, 0, id, full);
+        bulk_load(sb + scOff + (uint32_t)(c_lane * p.bs * 4),
                   p.kv + (int64_t)id * p.bs * (kDim + 4) + (int64_t)p.bs * kDim,
                   (uint32_t)p.bs * 4, full);
       }
@@ -537,19 +472,19 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         // accumulator a free again: the epilogue is done with the tile that
         // used it
         if (around > 0) {
-          if (!wait_phase(bar_acce + 8 * a, (uint32_t)((around - 1) & 1))) {
+          if (!mbar_wait_sleep(bar_acce + 8 * a, (uint32_t)((around - 1) & 1))) {
             *abort_flag = 1;
             report(p.err, kErrTimeoutBit);
             break;
           }
         }
         // tile n's data, or the producer's end marker covering tile n
-        int state = test_wait(bar_full + 8 * s, (uint32_t)(round & 1)) ? 1 : 0;
-        const uint64_t t0 = gtime();
+        int state = mbar_test_wait(bar_full + 8 * s, (uint32_t)(round & 1)) ? 1 : 0;
+        const uint64_t t0 = global_ns();
         while (state == 0) {
-          if (try_wait(bar_full + 8 * s, (uint32_t)(round & 1), 1000u)) state = 1;
+          if (mbar_try_wait_sleep(bar_full + 8 * s, (uint32_t)(round & 1), 1000u)) state = 1;
           else if (n >= *end_tile || *abort_flag) state = 2;
-          else if (gtime() - t0 > kWaitNs) state = 3;
+          else if (global_ns() - t0 > kWaitLimitNs) state = 3;
         }
         if (state == 3) {
           *abort_flag = 1;
@@ -561,7 +496,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
         if (d.b < 0) break;                             // the end marker's stage
         const int qs = (int)(d.qinfo & 1u);
         if ((d.qinfo & 3u) != seen_q) {         // a new query slot: wait for its rows
-          if (!wait_phase(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
+          if (!mbar_wait_sleep(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
             *abort_flag = 1;
             report(p.err, kErrTimeoutBit);
             break;
@@ -607,12 +542,12 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       // wait for tile n's accumulator, or for the end marker to cover tile n
       // (only the group holding the end tile is woken through the barrier)
       int state = 0;
-      const uint64_t t0 = gtime();
-      if (test_wait(bar_accf + 8 * a, (uint32_t)(around & 1))) state = 1;
+      const uint64_t t0 = global_ns();
+      if (mbar_test_wait(bar_accf + 8 * a, (uint32_t)(around & 1))) state = 1;
       while (state == 0) {
-        if (try_wait(bar_accf + 8 * a, (uint32_t)(around & 1), 1000u)) state = 1;
+        if (mbar_try_wait_sleep(bar_accf + 8 * a, (uint32_t)(around & 1), 1000u)) state = 1;
         else if (n >= *end_tile || *abort_flag) state = 2;
-        else if (gtime() - t0 > kWaitNs) state = 3;
+        else if (global_ns() - t0 > kWaitLimitNs) state = 3;
       }
       if (state == 3) {
         *abort_flag = 1;
@@ -623,7 +558,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       // the stage's full barrier has completed for this tile (its refill
       // waits for this group's four warps, below): waiting on it again makes
       // the producer's descriptor and the copied scales visible here
-      if (!wait_phase(bar_full + 8 * s, (uint32_t)(round & 1))) {
+      if (!mbar_wait_sleep(bar_full + 8 * s, (uint32_t)(round & 1))) {
         *abort_flag = 1;
         report(p.err, kErrTimeoutBit);
         break;
@@ -631,7 +566,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       const TileDesc d = desc[s];
       const int qs = (int)(d.qinfo & 1u);
       if ((d.qinfo & 3u) != seen_q) {            // a new query slot: its weights visible
-        if (!wait_phase(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
+        if (!mbar_wait_sleep(bar_qfull + 8 * qs, (d.qinfo >> 1) & 1u)) {
           *abort_flag = 1;
           report(p.err, kErrTimeoutBit);
           break;
@@ -646,7 +581,7 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       const bool missing = (d.missing >> (row >> p.bs_log2)) & 1u;
       const int64_t t = (int64_t)d.tile * kTile + row;
       __syncwarp();                              // every lane has its scale and the descriptor
-      if (lane == 0) bar_arrive(bar_empty + 8 * s);   // the stage may be refilled
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the stage may be refilled
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N);
       float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -661,8 +596,8 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        bar_arrive(bar_acce + 8 * a);
-        if (d.qinfo & 4u) bar_arrive(bar_qempty + 8 * qs);
+        mbar_arrive(bar_acce + 8 * a);
+        if (d.qinfo & 4u) mbar_arrive(bar_qempty + 8 * qs);
       }
       const int64_t cb = ctxc[d.b];
 #pragma unroll
@@ -690,13 +625,13 @@ logits_kernel(const LogitParams p, const __grid_constant__ CUtensorMap kmap,
     if (warp == 0 && lane == 0) {
       const int64_t first = issued > S ? issued - S : 0;
       for (int64_t m = first; m < issued; ++m)
-        wait_phase(bar_full + 8 * (int)(m % S), (uint32_t)((m / S) & 1));
+        mbar_wait_sleep(bar_full + 8 * (int)(m % S), (uint32_t)((m / S) & 1));
       for (int g = segs > 2 ? segs - 2 : 0; g < segs; ++g)
-        wait_phase(bar_qfull + 8 * (g & 1), (uint32_t)((g >> 1) & 1));
+        mbar_wait_sleep(bar_qfull + 8 * (g & 1), (uint32_t)((g >> 1) & 1));
     }
     if ((warp == 1 || warp >= 2 + kEpiWarps) && lane == 0 && last_issued >= 0) {
       const int64_t m = last_issued;
-      wait_phase(bar_accf + 8 * (int)(m % NA), (uint32_t)((m / NA) & 1));
+      mbar_wait_sleep(bar_accf + 8 * (int)(m % NA), (uint32_t)((m / NA) & 1));
     }
     __syncthreads();
   }

@@ -64,7 +64,6 @@ constexpr size_t kTableBytes = (size_t)(4 * kMaxRows + 1) * sizeof(int) +
 constexpr size_t kScoreSmem = (size_t)kRingBytes + 1024 + 2 * kMaxStages * 8 +
                               kMaxStages * 16 + kTableBytes;
 static_assert(kScoreSmem <= 227 * 1024 - 256, "score kernel shared memory");
-constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s: any wait longer is a fault
 
 constexpr int kTopkThreads = 512;                       // one key per thread in the sort
 
@@ -88,65 +87,6 @@ __device__ __forceinline__ RowSetup row_setup(const SelectParams& p, int r) {
   s.V = v > 0 ? v : 0;
   s.tail_end = pos < L - 1 ? pos : L - 1;
   return s;
-}
-
-// --- mbarrier / TMA helpers (sm_90+ PTX) -------------------------------------
-
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase of the given parity to complete; gives up after
-// kWaitLimitNs (returns false) so a lost copy can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
-  if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return true;
-}
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t mbar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
 }
 
 // acc + a*b with fp16 operands and a binary32 accumulator (one rounding; the
