@@ -33,7 +33,7 @@ Span span(const void* p, int64_t bytes) {
 
 bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
 
-constexpr int64_t kMaxRows = 65535;   // grid.y limit of the row-parallel kernels
+constexpr int64_t kMaxRows = 65535;   // rows per call (keeps every grid dimension in range)
 
 // Selection arguments (everything but the workspace): contract constants,
 // dtypes, shapes, strides, null pointers, alignment.  On success fills *p
