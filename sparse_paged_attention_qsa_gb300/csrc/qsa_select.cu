@@ -11,13 +11,13 @@
 //   score_kernel  persistent (one CTA per SM): streams every visible
 //                 compressed page of every row once through a TMA ring in
 //                 shared memory (the dominant HBM stream: 256 B per key) and
-//                 writes a 32-bit ordered score key per block to the
-//                 workspace;
-//   topk_kernel   one CTA per row: a lower bound of the 512-th largest key
-//                 from the per-thread maxima of one sweep, the keys reaching
-//                 it as candidates (a second sweep), exact radix select of
-//                 the top 512 over them, ordering of the winners, expansion,
-//                 tail and -1 padding.
+//                 writes a 32-bit ordered score key per block, and the
+//                 largest key of each run of 16 blocks, to the workspace;
+//   topk_kernel   one CTA per row: the candidates (every key of a short
+//                 row; for a long row the keys of the runs whose maximum
+//                 reaches a lower bound of the 512-th largest), exact radix
+//                 select of the top 512 over them, ordering of the winners,
+//                 expansion, tail and -1 padding.
 //
 // Score arithmetic (must match the oracle bit for bit): per head, four
 // 32-dim slices; in each slice an even-dim and an odd-dim binary32 chain
@@ -526,27 +526,30 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
 // ---------------------------------------------------------------------------
 //
 // One CTA per row.  Keys are bits(score)+1 (bit 31 clear, 0 = no key).
-//  1. One sweep (16-byte loads, eight in flight per thread) counts the keys
-//     and takes each thread's maximum and the row's maximum M; a row of at
-//     most 8192 blocks also keeps every key, with its block index, as a
-//     candidate in shared memory (one shared atomic per warp and step).
-//  2. A longer row: if at least K = min(512, #keys) threads hold a key, the
-//     smallest of their maxima is a lower bound L0 of the K-th largest key
-//     (K distinct keys -- the maxima -- are >= it), else L0 = 1; a second
-//     sweep keeps the keys >= L0 (about 9 % of a 32768-key row).
-//  3. Radix select over the candidates' offsets from their lower bound finds
-//     T, the K-th largest key, and `need`, how many keys equal to T belong to
-//     the top K.
-//     If more than `need` keys equal T, a second select over (2^31-1 - block
-//     index) of those ties keeps the `need` smallest block indices (the tie
-//     rule).
-//  4. The K (key, ~index) pairs are ordered (a bitonic sort of 512 slots),
+//  1. Candidates.  A row of at most kCandCap blocks takes every key, with
+//     its block index, into the candidate list (one load round up to 4096
+//     keys); K = min(512, #keys).  A longer row first reads its unit maxima
+//     (the largest key of each run of 16 blocks, written by the score
+//     kernel; staged in shared memory up to kUnitCap runs): with at least
+//     512 nonzero maxima, one 12-bit radix digit over [min, max] gives a
+//     lower bound lo of their 512-th largest, which bounds the 512-th
+//     largest key from below (512 distinct keys, the maxima, reach it);
+//     else lo = 1.  The runs whose maximum reaches lo (about 520 of 2048
+//     on a 32768-key row) are read (64 B each) and their keys >= lo are
+//     the candidates (about 590).
+//  2. Radix select over the candidates' offsets from lo finds T, the K-th
+//     largest key, and `need`, how many keys equal to T belong to the top
+//     K.  If more than `need` keys equal T, a second select over (2^31-1 -
+//     block index) of those ties keeps the `need` smallest block indices
+//     (the tie rule).
+//  3. The K (key, ~index) pairs are ordered (a bitonic sort of 512 slots),
 //     expanded, tail appended.
 // Every select takes 12-bit digits of (x - lo) from the top bit of hi - lo
 // down, so its first digit already spreads the members over the range they
 // span, and stops at the first digit whose bin holds exactly the members
-// still needed.  A row whose candidates still overflow the list falls back
-// to the same select over all of its keys, re-read from the workspace.
+// still needed.  A row whose hit runs or candidates overflow their lists
+// falls back to the same select over all of its keys, re-read from the
+// workspace.
 
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 8192;                          // candidate (key, block) pairs
@@ -718,8 +721,11 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
 
 // Top-k of row r by the CTA's kTopkThreads threads into `sh`.  The CTA
 // runs in the top-k kernel, a programmatic dependent of the score kernel,
-// and waits for it after the row's setup.  Ends after its last write of
-// p.out (no final barrier).
+// and waits for it after the row's setup.  kDense: every row of the launch
+// has at most kCandCap blocks (the page table is at most kCandCap / 128
+// columns wide), and all of a row's keys are its candidates.  Ends after its
+// last write of p.out (no final barrier).
+template <bool kDense>
 __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31;
   const RowSetup rs = row_setup(p, r);
@@ -746,113 +752,168 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
   __syncthreads();
   pdl_wait();      // the score kernel's keys are complete and visible
 
-  // 1. unit maxima: how many are nonzero, the smallest nonzero, the largest
-  // (M, the row's largest key); staged in shared memory
-  uint32_t nz = 0, umin = 0xffffffffu, M = 0;
-  {
-    const uint4* u4 = reinterpret_cast<const uint4*>(ur);
-    const int64_t nu4 = (nu + 3) >> 2;                   // the last vector may pass nu
-    for (int64_t b = tid; b < nu4; b += 2 * kTopkThreads) {
-      uint4 v[2];
+  // The candidates: a row of at most kCandCap keys takes all of them (one
+  // load round); a longer row the keys that reach a lower bound of its
+  // 512-th largest, found from the unit maxima.
+  uint32_t lo = 1u, M = 0, K = 0;
+  int ncand = 0;
+  bool fits = true;
+  if (kDense) {
+    // 1'. every key a candidate (block index = position); the largest key M
+    // and the count of keys (nonzero) give K = min(512, keys)
+    uint32_t nz = 0;
+    {
+      const uint4* s4 = reinterpret_cast<const uint4*>(sc);
+      const int64_t n4 = (Vs + 3) >> 2;                  // the last vector may pass Vs
+      constexpr int kPer = 2;                            // vectors per thread and round
+      for (int64_t b = tid; b < n4; b += kPer * kTopkThreads) {   // one round up to 4096 keys
+        uint4 v[kPer];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t i = b + (int64_t)u * kTopkThreads;
-        v[u] = i < nu4 ? ld_cg16(u4 + i) : make_uint4(0, 0, 0, 0);
-      }
+        for (int u = 0; u < kPer; ++u) {
+          const int64_t i = b + (int64_t)u * kTopkThreads;
+          v[u] = i < n4 ? ld_cg16(s4 + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t g0 = 4 * (b + (int64_t)u * kTopkThreads);
+        for (int u = 0; u < kPer; ++u) {
+          const int64_t g0 = 4 * (b + (int64_t)u * kTopkThreads);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t x = g0 + j < nu ? u4_at(v[u], j) : 0u;
-          if (u_in_smem && g0 + j < nu) sh.umax[g0 + j] = x;
-          nz += x != 0u;
-          umin = x != 0u && x < umin ? x : umin;
-          M = x > M ? x : M;
+          for (int j = 0; j < 4; ++j) {
+            if (g0 + j < Vs) {
+              const uint32_t x = u4_at(v[u], j);
+              sh.cand_x[g0 + j] = x;
+              sh.cand_i[g0 + j] = (uint32_t)(g0 + j);
+              nz += x != 0u;
+              M = x > M ? x : M;
+            }
+          }
         }
       }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      nz += __shfl_xor_sync(0xffffffffu, nz, o);
-      umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, o));
-      M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
-    }
-    if (lane == 0) {
-      sh.wsum[warp] = nz;
-      sh.wmin[warp] = umin;
-      sh.wmax[warp] = M;
-    }
-    __syncthreads();
-    nz = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      nz += sh.wsum[w];
-      umin = min(umin, sh.wmin[w]);
-      M = max(M, sh.wmax[w]);
-    }
-  }
-  // With >= 512 nonzero maxima (>= 512 keys), a lower bound of their 512-th
-  // largest -- one digit pass -- bounds the 512-th largest key from below
-  const bool many = nz >= (uint32_t)kTopkBlocks;
-  const uint32_t lo =
-      many ? radix_select<false, false>(sh, usrc, nu, kTopkBlocks, umin, M, 0u, 1).T : 1u;
-
-  // 2. units whose maximum reaches lo (listed in the histogram space), then
-  // their keys >= lo into the candidate list; one shared atomic per warp and
-  // step
-  uint32_t* hit = sh.hist;
-  for (int64_t base = 0; base < nu; base += 8 * kTopkThreads) {
-    uint32_t mask = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int64_t c = base + (int64_t)u * kTopkThreads + tid;
-      mask |= (uint32_t)(c < nu && usrc[c] >= lo) << u;   // lo >= 1: nonzero maxima only
-    }
-    int slot = warp_reserve(&sh.nhit, __popc(mask), lane);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (mask >> u & 1u) {
-        if (slot < kBins) hit[slot] = (uint32_t)(base + (int64_t)u * kTopkThreads + tid);
-        ++slot;
+      for (int o = 16; o > 0; o >>= 1) {
+        nz += __shfl_xor_sync(0xffffffffu, nz, o);
+        M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
+      }
+      if (lane == 0) {
+        sh.wsum[warp] = nz;
+        sh.wmax[warp] = M;
+      }
+      __syncthreads();
+      nz = 0;
+      for (int w = 0; w < kTopkWarps; ++w) {
+        nz += sh.wsum[w];
+        M = max(M, sh.wmax[w]);
       }
     }
-  }
-  __syncthreads();
-  const int nhit = sh.nhit;
-  if (nhit <= kBins) {
-    for (int base = 0; base < nhit; base += kTopkThreads) {
-      const int h = base + tid;
-      const int64_t g = h < nhit ? (int64_t)hit[h] : -1;
-      uint4 v[4];
+    ncand = (int)Vs;
+    K = nz < (uint32_t)kTopkBlocks ? nz : (uint32_t)kTopkBlocks;
+  } else {
+    // 1. unit maxima: how many are nonzero, the smallest nonzero, the largest
+    // (M, the row's largest key); staged in shared memory
+    uint32_t nz = 0, umin = 0xffffffffu;
+    {
+      const uint4* u4 = reinterpret_cast<const uint4*>(ur);
+      const int64_t nu4 = (nu + 3) >> 2;                   // the last vector may pass nu
+      for (int64_t b = tid; b < nu4; b += 2 * kTopkThreads) {
+        uint4 v[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        v[j] = g >= 0 ? ld_cg16(sc + kUnitKeys * g + 4 * j) : make_uint4(0, 0, 0, 0);
-      uint32_t mask = 0;                                   // bit j: key j of the unit
+        for (int u = 0; u < 2; ++u) {
+          const int64_t i = b + (int64_t)u * kTopkThreads;
+          v[u] = i < nu4 ? ld_cg16(u4 + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-      for (int j = 0; j < kUnitKeys; ++j) {
-        const uint32_t x = g >= 0 && kUnitKeys * g + j < Vs ? u4_at(v[j >> 2], j & 3) : 0u;
-        mask |= (uint32_t)(x >= lo) << j;
-      }
-      int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
+        for (int u = 0; u < 2; ++u) {
+          const int64_t g0 = 4 * (b + (int64_t)u * kTopkThreads);
 #pragma unroll
-      for (int j = 0; j < kUnitKeys; ++j) {
-        if (mask >> j & 1u) {
-          if (slot < kCandCap) {
-            sh.cand_x[slot] = u4_at(v[j >> 2], j & 3);
-            sh.cand_i[slot] = (uint32_t)(kUnitKeys * g + j);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t x = g0 + j < nu ? u4_at(v[u], j) : 0u;
+            if (u_in_smem && g0 + j < nu) sh.umax[g0 + j] = x;
+            nz += x != 0u;
+            umin = x != 0u && x < umin ? x : umin;
+            M = x > M ? x : M;
           }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        nz += __shfl_xor_sync(0xffffffffu, nz, o);
+        umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, o));
+        M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
+      }
+      if (lane == 0) {
+        sh.wsum[warp] = nz;
+        sh.wmin[warp] = umin;
+        sh.wmax[warp] = M;
+      }
+      __syncthreads();
+      nz = 0;
+      for (int w = 0; w < kTopkWarps; ++w) {
+        nz += sh.wsum[w];
+        umin = min(umin, sh.wmin[w]);
+        M = max(M, sh.wmax[w]);
+      }
+    }
+    // With >= 512 nonzero maxima (>= 512 keys), a lower bound of their 512-th
+    // largest -- one digit pass -- bounds the 512-th largest key from below
+    const bool many = nz >= (uint32_t)kTopkBlocks;
+    lo = many ? radix_select<false, false>(sh, usrc, nu, kTopkBlocks, umin, M, 0u, 1).T : 1u;
+
+    // 2. units whose maximum reaches lo (listed in the histogram space), then
+    // their keys >= lo into the candidate list; one shared atomic per warp and
+    // step
+    uint32_t* hit = sh.hist;
+    for (int64_t base = 0; base < nu; base += 8 * kTopkThreads) {
+      uint32_t mask = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t c = base + (int64_t)u * kTopkThreads + tid;
+        mask |= (uint32_t)(c < nu && usrc[c] >= lo) << u;   // lo >= 1: nonzero maxima only
+      }
+      int slot = warp_reserve(&sh.nhit, __popc(mask), lane);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (mask >> u & 1u) {
+          if (slot < kBins) hit[slot] = (uint32_t)(base + (int64_t)u * kTopkThreads + tid);
           ++slot;
         }
       }
     }
+    __syncthreads();
+    const int nhit = sh.nhit;
+    if (nhit <= kBins) {
+      for (int base = 0; base < nhit; base += kTopkThreads) {
+        const int h = base + tid;
+        const int64_t g = h < nhit ? (int64_t)hit[h] : -1;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[j] = g >= 0 ? ld_cg16(sc + kUnitKeys * g + 4 * j) : make_uint4(0, 0, 0, 0);
+        uint32_t mask = 0;                                   // bit j: key j of the unit
+#pragma unroll
+        for (int j = 0; j < kUnitKeys; ++j) {
+          const uint32_t x = g >= 0 && kUnitKeys * g + j < Vs ? u4_at(v[j >> 2], j & 3) : 0u;
+          mask |= (uint32_t)(x >= lo) << j;
+        }
+        int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
+#pragma unroll
+        for (int j = 0; j < kUnitKeys; ++j) {
+          if (mask >> j & 1u) {
+            if (slot < kCandCap) {
+              sh.cand_x[slot] = u4_at(v[j >> 2], j & 3);
+              sh.cand_i[slot] = (uint32_t)(kUnitKeys * g + j);
+            }
+            ++slot;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    ncand = sh.ncand;
+    fits = nhit <= kBins && ncand <= kCandCap;
+    // K = min(512, #keys): with >= 512 nonzero maxima there are >= 512 keys;
+    // otherwise every key is a candidate (fewer than 512 units hold keys)
+    K = many ? (uint32_t)kTopkBlocks
+             : (ncand < kTopkBlocks ? (uint32_t)ncand : (uint32_t)kTopkBlocks);
   }
-  __syncthreads();
-  const int ncand = sh.ncand;
-  const bool fits = nhit <= kBins && ncand <= kCandCap;
-  // K = min(512, #keys): with >= 512 nonzero maxima there are >= 512 keys;
-  // otherwise every key is a candidate (fewer than 512 units hold keys)
-  const uint32_t K = many ? (uint32_t)kTopkBlocks
-                          : (ncand < kTopkBlocks ? (uint32_t)ncand : (uint32_t)kTopkBlocks);
   const uint32_t tie_lo = 0x80000000u - (uint32_t)Vs;      // 2^31-1 - (Vs-1)
 
   if (K > 0) {
@@ -946,12 +1007,13 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
   }
 }
 
+template <bool kDense>
 __global__ void __launch_bounds__(kTopkThreads, 2)
 topk_kernel(const SelectParams p) {
   extern __shared__ __align__(16) unsigned char topk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   pdl_trigger();   // a dependent (the attention kernel) may be scheduled early (it waits)
-  topk_row(p, blockIdx.x, sh);
+  topk_row<kDense>(p, blockIdx.x, sh);
 }
 
 }  // namespace
@@ -1021,9 +1083,10 @@ cudaError_t device_info(DeviceInfo** out) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
       if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kTopkSmem);
-    if (e != cudaSuccess) return e;
+    for (auto k : {topk_kernel<false>, topk_kernel<true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
+      if (e != cudaSuccess) return e;
+    }
     d.smem_set = true;
   }
   *out = &d;
@@ -1056,7 +1119,11 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
       score_kernel<true><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
     else
       score_kernel<false><<<grid, kScoreThreads, kScoreSmem, stream>>>(c, map);
-    e = launch_after(topk_kernel, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c);
+    // rows of at most kCandCap blocks (every row, when the page table is
+    // that narrow) take all their keys as candidates
+    e = c.vcap <= kCandCap
+            ? launch_after(topk_kernel<true>, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c)
+            : launch_after(topk_kernel<false>, dim3(c.R), dim3(kTopkThreads), kTopkSmem, stream, c);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
