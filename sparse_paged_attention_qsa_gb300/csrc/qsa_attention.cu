@@ -56,12 +56,25 @@ attn_partial_kernel(const AttentionParams p) {
   __shared__ uint32_t sm_tok[kAttWarps][kWarpEntries];
 
   pdl_trigger();   // the combine kernel may be scheduled early (it waits)
-  pdl_wait();      // launched as a dependent of the previous kernel (the selection's
-                   // top-k when called after it): its output is complete and visible
-  const int req = p.t2r[r];
+  // Launched as a dependent of the previous kernel on the stream (the
+  // selection's top-k when called after it), whose output -- the index
+  // list -- is complete and visible only after pdl_wait().  When that
+  // kernel is known to write nothing else the attention reads, the request
+  // id, the query and the request's page-table row are fetched first.
+  int req = 0;
+  if (p.inputs_early) {
+    req = p.t2r[r];
+    attn::stage_query(p, r, qf, tid, kAttThreads);
+    if (tid == 0 && req >= 0 && req < p.num_reqs)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.pt + (int64_t)req * p.pt_stride0));
+  }
+  pdl_wait();
+  if (!p.inputs_early) {
+    req = p.t2r[r];
+    attn::stage_query(p, r, qf, tid, kAttThreads);
+  }
   const bool rok = req >= 0 && req < p.num_reqs;
   if (!rok && split == 0 && tid == 0) report(p.err, kErrRequest);
-  attn::stage_query(p, r, qf, tid, kAttThreads);
   const int nvalid = attn::resolve_entries<kWarpEntries>(
       p, r, req, rok, (int64_t)split * kSplit + warp * kWarpEntries, sm_tok[warp], lane);
   __syncthreads();   // the query fragments are staged

@@ -68,6 +68,8 @@ struct AttentionParams {
   int nsplit;
   uint32_t* err;              // nullable
   int R;
+  int inputs_early;           // 1: the kernel before it on the stream writes none of q,
+                              // t2r, pt (only idx), so they may be read before its end
 };
 
 // Launch `kernel` so that it may start while the previous kernel in the

@@ -1142,6 +1142,7 @@ cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a
   ac.idx_stride0 = p.out_stride0;
   ac.width = kOutWidth;
   ac.nsplit = attention_splits(p.R, kOutWidth);
+  ac.inputs_early = 1;   // the kernel before it is the top-k, which writes only the indices
   return launch_attention(ac, stream);
 }
 
