@@ -107,6 +107,21 @@ def test_select_rows_longer_than_the_staged_unit_maxima():
     _check(w)
 
 
+@pytest.mark.parametrize("cols", [64, 65])
+@pytest.mark.parametrize("distinct", [0, 3])
+def test_select_short_row_top_k_boundary(cols, distinct):
+    # a page table of at most 64 columns (every row <= 8192 blocks) takes the
+    # top-k that loads all of a row's keys as candidates; 65 columns the one
+    # that goes through the unit maxima -- both bit-exact at the boundary
+    # (rows of exactly 8192 blocks, shorter rows, ties)
+    lens = [32768, 32768 + 3, 32767, 8195, 2051]
+    w = W.build("cols", lens, cmp_cols=cols, distinct_keys=distinct, seed=40 + cols + distinct,
+                device=DEV)
+    assert w.cmp_page_table.shape[1] == cols
+    _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
 def test_select_all_zero_scores_long_row():
     # every key equals bits(+0)+1: 32768 ties, kept in block order
     w = W.build("zeros_long", [131072], seed=14, device=DEV)
