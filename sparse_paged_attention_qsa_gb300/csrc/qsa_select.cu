@@ -1133,7 +1133,7 @@ cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a
                                  cudaStream_t stream) {
   // the selection's kernels, then the attention's over its output, all on
   // the caller's stream; the top-k is a programmatic dependent of the score
-  // kernel, and the attention of batches of up to 16 rows of the top-k
+  // kernel, and the attention of batches of up to 32 rows of the top-k
   if (p.R == 0) return cudaSuccess;
   cudaError_t e = launch_select(p, stream);
   if (e != cudaSuccess) return e;

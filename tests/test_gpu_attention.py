@@ -93,9 +93,9 @@ def test_attention_config4_full_size_sampled_rows():
     assert np.isfinite(got).all()
 
 
-@pytest.mark.parametrize("R", [16, 17, 40])
+@pytest.mark.parametrize("R", [16, 32, 33, 40])
 def test_attention_batch_sizes_around_the_split_switch(R):
-    # batches of up to 16 rows take 64-entry splits, larger ones the stream
+    # batches of up to 32 rows take 64-entry splits, larger ones the stream
     # split: premade lists with holes and duplicates, every width, bad ids
     w = _lists(R, [0, 1, 32, 1024, 2051, 1500, 77], 3000, seed=60 + R)
     pt = w.kv_page_table.clone()
@@ -107,11 +107,11 @@ def test_attention_batch_sizes_around_the_split_switch(R):
     assert (got[R - 1] == 0).all()
 
 
-@pytest.mark.parametrize("R,L,width", [(17, 3000, 0), (17, 3000, 1), (40, 3000, 33),
+@pytest.mark.parametrize("R,L,width", [(33, 3000, 0), (33, 3000, 1), (40, 3000, 33),
                                         (97, 3000, 300), (300, 2100, 2051), (1100, 700, 2051),
                                         (1100, 700, 77)])
 def test_attention_stream_runs_across_rows(R, L, width):
-    # batches of more than 16 rows: the index lists cut into 32-entry chunks
+    # batches of more than 32 rows: the index lists cut into 32-entry chunks
     # laid end to end and split into equal runs, one per CTA of one wave; a
     # run spans two rows (or three at 1100 rows), a row several runs
     valid = [min(v, L) for v in (2051, 1500, 77, 0, 32, 513)]

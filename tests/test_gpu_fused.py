@@ -7,8 +7,8 @@ multi-request cases).
 
 The call runs the two calls' kernels from one workspace, so its outputs
 must equal the two calls' bit for bit.  The attention cuts the index lists
-differently on either side of 16 rows (64-entry splits, or equal runs over
-the batch): the edge cases run both ways (the row list repeated past 16
+differently on either side of 32 rows (64-entry splits, or equal runs over
+the batch): the edge cases run both ways (the row list repeated past 32
 rows), and the tests also cover row chunks (more than 1024 rows),
 speculative rows that share a request, and repeated calls on a dirty
 workspace.  Tolerance as in test_gpu_attention.py.
@@ -79,8 +79,8 @@ def test_fused_matches_two_call_path():
 
 
 def _rows(lens, big):
-    """The row list, repeated past 16 rows when the large-batch attention is wanted."""
-    return lens * (17 // len(lens) + 1) if big else lens
+    """The row list, repeated past 32 rows when the large-batch attention is wanted."""
+    return lens * (33 // len(lens) + 1) if big else lens
 
 
 @pytest.mark.parametrize("big", [False, True])
