@@ -145,6 +145,26 @@ def test_fused_more_rows_than_one_launch():
     assert gerr == 0
 
 
+def test_fused_maximum_rows_in_one_call():
+    # 65535 rows (the most one call takes) of one request at different
+    # positions: the selection runs in 64 row chunks, and each stream run of
+    # the attention spans some 200 rows; sampled rows against the oracle
+    R = 65535
+    base = W.build("maxrows", [3000], seed=95, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(96)
+    w = W.Workload(**{
+        **base.__dict__,
+        "R": R,
+        "q_sel": torch.randn((R, 4, 128), generator=g, device=DEV).half(),
+        "q_attn": torch.randn((R, 3, 256), generator=g, device=DEV).half(),
+        "token_to_request": torch.zeros(R, dtype=torch.int32, device=DEV),
+        "query_positions": torch.randint(0, 3000, (R,), generator=g, device=DEV,
+                                         dtype=torch.int64)})
+    _, got_out, gerr, oerr = _check(w, rows=[0, 1, 1023, 1024, 32767, 65533, 65534])
+    assert gerr == oerr == 0
+    assert np.isfinite(got_out).all()
+
+
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_fused_repeat_calls_on_dirty_workspace(cfg):
     w = W.config(cfg, device=DEV)
