@@ -263,19 +263,22 @@ qsa_status qsa_select_paged_tokens(
       compress_ratio, out_indices, out_dtype, out_width, out_stride0, error_word, &p, &o, ins,
       &empty);
   if (st != QSA_OK || empty) return st;
+  // aliasing among the caller's tensors first, then the workspace (so a call
+  // without a workspace still learns of every other argument error)
+  for (const Span& s : ins)
+    if (overlaps(o, s)) return QSA_ERR_ALIAS;
+  if (error_word) {
+    const Span e = span(error_word, 4);
+    if (overlaps(o, e)) return QSA_ERR_ALIAS;
+    for (const Span& s : ins)
+      if (overlaps(e, s)) return QSA_ERR_ALIAS;
+  }
   const size_t need = qsa::select_workspace_bytes(num_rows, cmp_pt_cols);
   if (!workspace || workspace_bytes < need) return QSA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return QSA_ERR_ALIGN;
   const Span ws = span(workspace, (int64_t)need);
   if (overlaps(o, ws)) return QSA_ERR_ALIAS;
-  for (const Span& s : ins)
-    if (overlaps(o, s)) return QSA_ERR_ALIAS;
-  if (error_word) {
-    const Span e = span(error_word, 4);
-    if (overlaps(o, e) || overlaps(e, ws)) return QSA_ERR_ALIAS;
-    for (const Span& s : ins)
-      if (overlaps(e, s)) return QSA_ERR_ALIAS;
-  }
+  if (error_word && overlaps(span(error_word, 4), ws)) return QSA_ERR_ALIAS;
   p.scores = static_cast<uint32_t*>(workspace);
   p.umax = p.scores + num_rows * p.vcap;
   const cudaError_t e = qsa::launch_select(p, reinterpret_cast<cudaStream_t>(stream));

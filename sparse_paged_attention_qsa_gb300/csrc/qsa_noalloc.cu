@@ -15,44 +15,33 @@
 // workspace.  All calls share the one array, so calls whose kernels overlap
 // on the GPU (other streams, other host threads) race and must be serialised
 // by the caller.  Every scratch slot a call reads is written earlier in the
-// same call, so nothing needs clearing between calls.
+// same call when its device waits complete, so nothing needs clearing
+// between calls (the timeout case is below).
 //
-// The host cannot use the array's name as a device address; the device
-// address is looked up with cudaGetSymbolAddress once per device, the first
-// time this entry point runs with that device current.  That first call may
-// also load the library's GPU code onto the device, so make it before any
-// stream capture.
+// The host cannot use the array's name as a device address.  Every call
+// looks the address up with cudaGetSymbolAddress in the context current at
+// the call (cheap, and it allocates nothing), so a reset device or another
+// context on the same ordinal never receives an address from an earlier
+// context.  The first call on a device may also load the library's GPU code
+// onto it, so make that first call before any stream capture.
+//
+// Validation comes first: the call is checked exactly as the workspace entry
+// point checks it (with no workspace, which makes a well-formed call stop at
+// the workspace check without launching), so a malformed call returns the
+// status that entry point gives; only a well-formed request larger than the
+// array returns QSA_ERR_SCRATCH_LIMIT.
+//
+// After a device wait gives up (QSA_DERR_TIMEOUT in the error word) the
+// scoring stopped early and the top-k may have read slots of the array that
+// an earlier call wrote; the indices of that call are undefined.
 #include "qsa.h"
 #include "qsa_internal.h"
-
-#include <mutex>
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = QSA_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_select_scratch[kStaticScratchBytes];
-
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_select_scratch on the current device (set up once).
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_select_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return cudaSuccess;
-}
 
 }  // namespace
 
@@ -69,19 +58,26 @@ qsa_status qsa_select_paged_tokens_static_scratch(
     qsa_dtype seq_lens_dtype, const void* query_positions, qsa_dtype qpos_dtype,
     int32_t token_topk, int32_t compress_ratio, void* out_indices, qsa_dtype out_dtype,
     int64_t out_width, int64_t out_stride0, uint32_t* error_word, qsa_stream_t stream) {
-  if (num_rows > 0 && cmp_pt_cols > 0 &&
-      qsa::select_workspace_bytes(num_rows, cmp_pt_cols) > kStaticScratchBytes)
+  // argument checks of the workspace entry point; with no workspace a
+  // well-formed, non-empty call stops at QSA_ERR_WORKSPACE, launching nothing
+  const qsa_status st = qsa_select_paged_tokens(
+      q_sel, q_sel_dtype, num_rows, q_sel_strides, cmp_cache, cmp_dtype, cmp_shape, cmp_strides,
+      cmp_page_table, cmp_pt_dtype, num_reqs, cmp_pt_cols, cmp_pt_stride0, token_to_request,
+      t2r_dtype, seq_lens, seq_lens_dtype, query_positions, qpos_dtype, token_topk,
+      compress_ratio, out_indices, out_dtype, out_width, out_stride0, nullptr, 0, error_word,
+      stream);
+  if (st != QSA_ERR_WORKSPACE) return st;    // an argument error, or an empty batch (QSA_OK)
+  if (qsa::select_workspace_bytes(num_rows, cmp_pt_cols) > kStaticScratchBytes)
     return QSA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  if (num_rows > 0) {
-    if (scratch_address(&scratch) != cudaSuccess) return QSA_ERR_CUDA;
-  }
+  if (cudaGetSymbolAddress(&scratch, g_select_scratch) != cudaSuccess || scratch == nullptr)
+    return QSA_ERR_CUDA;
   return qsa_select_paged_tokens(
       q_sel, q_sel_dtype, num_rows, q_sel_strides, cmp_cache, cmp_dtype, cmp_shape, cmp_strides,
       cmp_page_table, cmp_pt_dtype, num_reqs, cmp_pt_cols, cmp_pt_stride0, token_to_request,
       t2r_dtype, seq_lens, seq_lens_dtype, query_positions, qpos_dtype, token_topk,
       compress_ratio, out_indices, out_dtype, out_width, out_stride0, scratch,
-      scratch ? kStaticScratchBytes : 0, error_word, stream);
+      kStaticScratchBytes, error_word, stream);
 }
 
 }  // extern "C"

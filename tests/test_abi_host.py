@@ -127,6 +127,32 @@ def test_select_zero_rows_is_noop(lib):
     assert _sel(lib, R=0, ws=None, wsb=0) == 0
 
 
+def _static_sel(lib, **over):
+    """qsa_select_paged_tokens_static_scratch with _sel's arguments (no workspace pair)."""
+    R = over.pop("R", 4)
+    cols = over.pop("cols", 8)
+    a = dict(q=_addr(1), qdt=1, R=R, qs=_arr([512, 128, 1]),
+             cmp=_addr(2), cdt=1, cshape=_arr([64, 128, 1, 128]), cstr=_arr([16384, 128, 128, 1]),
+             pt=_addr(40), ptdt=4, nreq=R, cols=cols, pts0=cols,
+             t2r=_addr(50), t2rdt=4, sl=_addr(60), sldt=4, qp=_addr(70), qpdt=5,
+             topk=2048, ratio=4, out=_addr(80), odt=4, ow=2051, os0=2051, err=None, stream=None)
+    a.update(over)
+    return lib.qsa_select_paged_tokens_static_scratch(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    # malformed calls get the workspace entry point's status, whatever their size
+    (dict(R=70000), 3), (dict(cols=(1 << 20) + 1), 3), (dict(topk=1024, cols=4096), 6),
+    (dict(qdt=3, cols=4096), 2), (dict(q=None, cols=4096), 1), (dict(out=_addr(1), cols=4096), 8),
+    # a well-formed request beyond the array: the scratch limit, nothing launched
+    (dict(cols=4096), 10), (dict(R=1024, cols=64), 10),
+    (dict(R=0), 0),            # empty batch: a no-op
+])
+def test_static_scratch_validates_before_the_size_check(lib, over, status):
+    assert lib.qsa_static_scratch_bytes() == 4 << 20
+    assert _static_sel(lib, **over) == status
+
+
 # --- fail-closed attention --------------------------------------------------
 
 def _att(lib, **over):

@@ -7,7 +7,11 @@ inside the library instead of a caller workspace.
 Checks, through the C ABI: two calls in a row on each of several workloads
 give exactly the indices of qsa_select_paged_tokens (the workspace entry
 point); switching workloads between calls leaves no stale scratch behind;
-a request larger than the array is refused without launching.
+the calls allocate no device memory (the driver's free-memory figure and
+torch's allocator are unchanged across them); an empty batch returns OK and
+writes nothing; a request larger than the array is refused without
+launching, and a malformed one gets the workspace entry point's status, not
+the scratch-limit one.
 
 This file is collected last so a run that stops at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -24,6 +28,7 @@ from sparse_paged_attention_qsa_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 SCRATCH_LIMIT = 10   # QSA_ERR_SCRATCH_LIMIT
+SHAPE = 3            # QSA_ERR_SHAPE
 
 
 def _lib():
@@ -45,10 +50,10 @@ def _a(v):
     return (ctypes.c_int64 * len(v))(*v)
 
 
-def _static_select(lib, w, out, err, pt=None):
+def _static_select(lib, w, out, err, pt=None, rows=None):
     pt = w.cmp_page_table if pt is None else pt
     return lib.qsa_select_paged_tokens_static_scratch(
-        w.q_sel.data_ptr(), 1, w.R, _a(w.q_sel.stride()),
+        w.q_sel.data_ptr(), 1, w.R if rows is None else rows, _a(w.q_sel.stride()),
         w.cmp_cache.data_ptr(), 1, _a(w.cmp_cache.shape), _a(w.cmp_cache.stride()),
         pt.data_ptr(), 4, pt.shape[0], pt.shape[1], pt.stride(0),
         w.token_to_request.data_ptr(), 4, w.seq_lens.data_ptr(), 4,
@@ -91,3 +96,44 @@ def test_static_scratch_refuses_oversized_request():
     torch.cuda.synchronize()
     assert (out == -7).all()                  # nothing was launched
     assert b"static scratch" in lib.qsa_status_string(SCRATCH_LIMIT)
+
+
+def test_static_scratch_allocates_nothing():
+    lib = _lib()
+    w = W.build("mixed", [60001, 519, 33333, 9215], seed=24, device=DEV)
+    out = torch.full((w.R, 2051), -7, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _static_select(lib, w, out, err) == 0       # first call: any one-time set-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(5):
+        assert _static_select(lib, w, out, err) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert torch.cuda.memory_allocated() == alloc0
+    assert int(err.item()) == 0
+
+
+def test_static_scratch_empty_batch_writes_nothing():
+    lib = _lib()
+    w = W.build("small", [515] * 2, seed=25, device=DEV)
+    out = torch.full((2, 2051), -7, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _static_select(lib, w, out, err, rows=0) == 0
+    torch.cuda.synchronize()
+    assert (out == -7).all()
+    assert int(err.item()) == 0
+
+
+def test_static_scratch_malformed_call_gets_the_argument_status():
+    # 70000 rows is beyond the per-call row limit: the argument check answers
+    # (QSA_ERR_SHAPE) before the scratch size is looked at
+    lib = _lib()
+    w = W.build("small", [515] * 2, seed=26, device=DEV)
+    out = torch.full((2, 2051), -7, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _static_select(lib, w, out, err, rows=70000) == SHAPE
+    torch.cuda.synchronize()
+    assert (out == -7).all()
