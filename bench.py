@@ -226,6 +226,17 @@ class OracleSample:
         o.attention(self.qa[r:r + 1], self.kpool, self.kpt, self.t2r[r:r + 1], idx)
 
 
+def host_cores():
+    """(cores of the host, cores this process may run on): the oracle runs one
+    thread per usable core."""
+    total = os.cpu_count() or 1
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except Exception:
+        usable = total
+    return total, max(1, usable)
+
+
 def oracle_rate(sample: OracleSample, n_rows: int, threads: int):
     """Rows/s of the oracle over n_rows decode rows spread over `threads` OS
     threads (the C code releases the GIL); returns (rows/s, wall seconds)."""
@@ -255,7 +266,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     from sparse_paged_attention_qsa_gb300 import workloads as W
-    threads = max(1, min(os.cpu_count() or 1, 16))
+    total_cores, threads = host_cores()
     w = _sample_workload(args.workload, threads, rank)
     sample = OracleSample(w, range(min(threads, w.R)))
     del w
@@ -267,7 +278,8 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
         "data": "synthetic",
         "config": {"workload": W.CONFIG_NAMES[args.workload], "rows_per_step": 1},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads,
+                         "threads": threads, "host_cores": total_cores, "kind": "oracle",
                          "sample": f"{args.steps} decode rows (select+attend) cycling over "
                                    f"{len(sample.rows)} rows of {W.CONFIG_NAMES[args.workload]}, "
                                    f"plain C oracle on {threads} threads, {dt:.1f} s wall"},
@@ -447,14 +459,15 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        threads = max(1, min(os.cpu_count() or 1, 16))
+        total_cores, threads = host_cores()
         sample = OracleSample(w, range(min(threads, R)))
         rate0, _ = oracle_rate(sample, 2 * len(sample.rows), threads)   # calibration
         n = max(2 * len(sample.rows), int(rate0 * 10.0))                 # about 10 s of rows
         rate, dt = oracle_rate(sample, n, threads)
         n1 = max(2, int(rate / threads * 3.0))                           # about 3 s on one core
         rate1, _ = oracle_rate(sample, n1, 1)
-        cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": rate, "unit": "rows/s", "cores": threads, "threads": threads,
+               "host_cores": total_cores, "kind": "oracle",
                "single_thread_value": rate1,
                "sample": f"{n} decode rows (select+attend) over {len(sample.rows)} rows of "
                          f"this workload, plain C oracle on {threads} threads, {dt:.1f} s wall"}

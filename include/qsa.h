@@ -9,8 +9,9 @@
  *                             "Exact contracts" / Selection.
  *   qsa_sparse_attention      same page, Summary (exact-packed attention
  *                             bullet) and "Exact contracts" / Attention.
- *   qsa_select_attend         both in one call, the attention of early rows
- *                             overlapping the scoring of later ones.
+ *   qsa_select_attend         both in one call and one workspace: the two
+ *                             operations' kernels chained on the stream by
+ *                             programmatic dependent launch.
  *
  * The visible-block rule used by selection comes from qsa_cache.py
  * (_build_qsa_metadata_kernel: visible = max(0, min((pos+1)//4, seq_len//4))).
@@ -274,11 +275,21 @@ QSA_API qsa_status qsa_select_attend(
  * request returns QSA_ERR_SCRATCH_LIMIT without launching.  The call
  * allocates nothing.  All calls share the array: calls whose kernels overlap
  * on the GPU (different streams or host threads) race, so serialise them.
- * Nothing in the array needs clearing between calls.
+ * Nothing in the array needs clearing between calls: every slot a call
+ * reads is written earlier in the same call -- as long as the call's device
+ * waits complete.  If *error_word comes back with QSA_DERR_TIMEOUT, the
+ * scoring stopped early, the top-k may have read slots left by an earlier
+ * call (possibly of another workload), and out_indices is undefined; check
+ * the error word before using the indices.
  *
- * Set-up: the first call with a given device current looks up the array's
- * device address (cudaGetSymbolAddress) and may load the library's GPU code
- * onto that device; make that first call before any stream capture.
+ * Set-up: every call looks up the array's device address in the current
+ * context (cudaGetSymbolAddress; no allocation).  The first call on a
+ * device may also load the library's GPU code onto it; make that first call
+ * before any stream capture.
+ *
+ * Validation: the arguments are checked exactly as qsa_select_paged_tokens
+ * checks them (a malformed call returns that entry point's status); only a
+ * well-formed request larger than the array returns QSA_ERR_SCRATCH_LIMIT.
  *
  * Arguments, validation and results are those of qsa_select_paged_tokens
  * without the workspace pair.

@@ -66,75 +66,113 @@ def load_library(path: str | None = None):
                 f"libqsa.so not found at {path}; build it with "
                 "`python -m sparse_paged_attention_qsa_gb300.build` (nvcc, sm_103a)")
         lib = ctypes.CDLL(path)
-        i32, i64, u64, vp, sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
-                                 ctypes.c_void_p, ctypes.c_size_t)
-        p64 = ctypes.POINTER(ctypes.c_int64)
-        lib.qsa_status_string.restype = ctypes.c_char_p
-        lib.qsa_status_string.argtypes = [ctypes.c_int]
-        lib.qsa_version.restype = ctypes.c_int
-        lib.qsa_version.argtypes = []
-        lib.qsa_select_workspace_bytes.restype = sz
-        lib.qsa_select_workspace_bytes.argtypes = [i64, i64]
-        lib.qsa_attention_workspace_bytes.restype = sz
-        lib.qsa_attention_workspace_bytes.argtypes = [i64, i64]
-        lib.qsa_select_paged_tokens.restype = ctypes.c_int
-        lib.qsa_select_paged_tokens.argtypes = [
-            vp, ctypes.c_int, i64, p64,
-            vp, ctypes.c_int, p64, p64,
-            vp, ctypes.c_int, i64, i64, i64,
-            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
-            i32, i32,
-            vp, ctypes.c_int, i64, i64,
-            vp, sz, vp, vp]
-        lib.qsa_sparse_attention.restype = ctypes.c_int
-        lib.qsa_sparse_attention.argtypes = [
-            vp, ctypes.c_int, i64, p64,
-            vp, vp, ctypes.c_int, p64, p64, p64,
-            vp, ctypes.c_int, i64, i64, i64,
-            vp, ctypes.c_int,
-            vp, ctypes.c_int, i64, i64,
-            ctypes.c_float,
-            vp, ctypes.c_int, p64,
-            vp, sz, vp, vp]
-        lib.qsa_select_attend_workspace_bytes.restype = sz
-        lib.qsa_select_attend_workspace_bytes.argtypes = [i64, i64]
-        lib.qsa_select_attend.restype = ctypes.c_int
-        lib.qsa_select_attend.argtypes = [
-            vp, ctypes.c_int, i64, p64,
-            vp, ctypes.c_int, p64, p64,
-            vp, ctypes.c_int, i64, i64, i64,
-            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
-            i32, i32,
-            vp, ctypes.c_int, i64, i64,
-            vp, ctypes.c_int, p64,
-            vp, vp, ctypes.c_int, p64, p64, p64,
-            vp, ctypes.c_int, i64, i64,
-            ctypes.c_float,
-            vp, ctypes.c_int, p64,
-            vp, sz, vp, vp]
-        lib.qsa_build_metadata.restype = ctypes.c_int
-        lib.qsa_build_metadata.argtypes = [
-            vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
-            vp, ctypes.c_int, i64, i64, i64, i64,
-            i64, i64, i64, i64, i64, i64,
-            vp, vp, vp, vp, vp, i64, vp]
-        lib.qsa_paged_mqa_logits.restype = ctypes.c_int
-        lib.qsa_paged_mqa_logits.argtypes = [
-            vp, ctypes.c_int, i64, i64,
-            vp, ctypes.c_int, i64, i64,
-            vp, ctypes.c_int,
-            vp, ctypes.c_int, i64,
-            vp, ctypes.c_int, i64, i64,
-            i64,
-            vp, ctypes.c_int, i64, i64,
-            vp, vp]
-        lib.qsa_top_k_per_row_decode.restype = ctypes.c_int
-        lib.qsa_top_k_per_row_decode.argtypes = [
-            vp, ctypes.c_int, i64, i64, i64, i64, i64,
-            vp, ctypes.c_int, i64,
-            i64, vp, ctypes.c_int, i64, vp]
+        declare_signatures(lib)
         _lib = lib
         return lib
+
+
+class _Only:
+    """Attribute access on a library that may lack some entry points (a
+    test build carries a subset): missing ones are skipped."""
+
+    def __init__(self, lib):
+        self._lib = lib
+
+    def __getattr__(self, name):
+        try:
+            return getattr(self._lib, name)
+        except AttributeError:
+            return _Sink()
+
+
+class _Sink:
+    def __setattr__(self, name, value):
+        pass
+
+
+def declare_signatures(lib):
+    """Declare the C signatures of include/*.h on a loaded library handle."""
+    full = lib
+    lib = _Only(full)
+    i32, i64, u64, vp, sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                             ctypes.c_void_p, ctypes.c_size_t)
+    p64 = ctypes.POINTER(ctypes.c_int64)
+    lib.qsa_status_string.restype = ctypes.c_char_p
+    lib.qsa_status_string.argtypes = [ctypes.c_int]
+    lib.qsa_version.restype = ctypes.c_int
+    lib.qsa_version.argtypes = []
+    lib.qsa_select_workspace_bytes.restype = sz
+    lib.qsa_select_workspace_bytes.argtypes = [i64, i64]
+    lib.qsa_attention_workspace_bytes.restype = sz
+    lib.qsa_attention_workspace_bytes.argtypes = [i64, i64]
+    lib.qsa_select_paged_tokens.restype = ctypes.c_int
+    lib.qsa_select_paged_tokens.argtypes = [
+        vp, ctypes.c_int, i64, p64,
+        vp, ctypes.c_int, p64, p64,
+        vp, ctypes.c_int, i64, i64, i64,
+        vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+        i32, i32,
+        vp, ctypes.c_int, i64, i64,
+        vp, sz, vp, vp]
+    lib.qsa_static_scratch_bytes.restype = sz
+    lib.qsa_static_scratch_bytes.argtypes = []
+    lib.qsa_select_paged_tokens_static_scratch.restype = ctypes.c_int
+    lib.qsa_select_paged_tokens_static_scratch.argtypes = [
+        vp, ctypes.c_int, i64, p64,
+        vp, ctypes.c_int, p64, p64,
+        vp, ctypes.c_int, i64, i64, i64,
+        vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+        i32, i32,
+        vp, ctypes.c_int, i64, i64,
+        vp, vp]
+    lib.qsa_sparse_attention.restype = ctypes.c_int
+    lib.qsa_sparse_attention.argtypes = [
+        vp, ctypes.c_int, i64, p64,
+        vp, vp, ctypes.c_int, p64, p64, p64,
+        vp, ctypes.c_int, i64, i64, i64,
+        vp, ctypes.c_int,
+        vp, ctypes.c_int, i64, i64,
+        ctypes.c_float,
+        vp, ctypes.c_int, p64,
+        vp, sz, vp, vp]
+    lib.qsa_select_attend_workspace_bytes.restype = sz
+    lib.qsa_select_attend_workspace_bytes.argtypes = [i64, i64]
+    lib.qsa_select_attend.restype = ctypes.c_int
+    lib.qsa_select_attend.argtypes = [
+        vp, ctypes.c_int, i64, p64,
+        vp, ctypes.c_int, p64, p64,
+        vp, ctypes.c_int, i64, i64, i64,
+        vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+        i32, i32,
+        vp, ctypes.c_int, i64, i64,
+        vp, ctypes.c_int, p64,
+        vp, vp, ctypes.c_int, p64, p64, p64,
+        vp, ctypes.c_int, i64, i64,
+        ctypes.c_float,
+        vp, ctypes.c_int, p64,
+        vp, sz, vp, vp]
+    lib.qsa_build_metadata.restype = ctypes.c_int
+    lib.qsa_build_metadata.argtypes = [
+        vp, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+        vp, ctypes.c_int, i64, i64, i64, i64,
+        i64, i64, i64, i64, i64, i64,
+        vp, vp, vp, vp, vp, i64, vp]
+    lib.qsa_paged_mqa_logits.restype = ctypes.c_int
+    lib.qsa_paged_mqa_logits.argtypes = [
+        vp, ctypes.c_int, i64, i64,
+        vp, ctypes.c_int, i64, i64,
+        vp, ctypes.c_int,
+        vp, ctypes.c_int, i64,
+        vp, ctypes.c_int, i64, i64,
+        i64,
+        vp, ctypes.c_int, i64, i64,
+        vp, vp]
+    lib.qsa_top_k_per_row_decode.restype = ctypes.c_int
+    lib.qsa_top_k_per_row_decode.argtypes = [
+        vp, ctypes.c_int, i64, i64, i64, i64, i64,
+        vp, ctypes.c_int, i64,
+        i64, vp, ctypes.c_int, i64, vp]
+    return full
 
 
 def _arr(vals):
@@ -177,9 +215,10 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 def qsa_select_paged_tokens(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
                             query_positions, token_topk: int = TOKEN_TOPK,
                             compress_ratio: int = COMPRESS_RATIO, out=None, workspace=None,
-                            error_word=None, stream=None):
-    """Selection: returns out [R,2051] int32 (see include/qsa.h)."""
-    lib = load_library()
+                            error_word=None, stream=None, library=None):
+    """Selection: returns out [R,2051] int32 (see include/qsa.h).  `library`:
+    another loaded build of the C ABI (declare_signatures) instead of libqsa."""
+    lib = library or load_library()
     R = q_sel.shape[0] if q_sel.dim() == 3 else -1
     if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
         raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
@@ -271,12 +310,12 @@ def qsa_select_attend_workspace_bytes(num_rows: int, cmp_pt_cols: int) -> int:
 def qsa_select_attend(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
                       query_positions, q_attn, k_cache, v_cache, kv_page_table,
                       scale: float = 1.0 / 16.0, indices=None, out=None, workspace=None,
-                      error_word=None, stream=None):
+                      error_word=None, stream=None, library=None):
     """One decode step in one call (include/qsa.h, qsa_select_attend): the
     selection's indices [R,2051] int32 and the attention output [R,3,256]
-    FP16, with the attention of early rows overlapping the scoring of later
-    ones.  Both page tables are indexed by token_to_request."""
-    lib = load_library()
+    FP16.  Both page tables are indexed by token_to_request.  `library` as in
+    qsa_select_paged_tokens."""
+    lib = library or load_library()
     if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
         raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
     if q_attn.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or kv_page_table.dim() != 2:
