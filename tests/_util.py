@@ -1,10 +1,34 @@
 """Shared test helpers: run the oracle on a workload's tensors (copied to the
 host) and run the CUDA path through the binding.  The oracle receives only the
 pages the checked rows reference, so full-size pools never leave the GPU."""
+import os
+
 import numpy as np
 import torch
 
 import oracle
+
+# oracle threads for full-size checks: one per usable host core
+CORES = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+            else (os.cpu_count() or 1))
+
+
+def stream_edge_rows(R: int, width: int, sms: int, ctas_per_sm: int = 2):
+    """Rows of a batch of more than 32 rows whose index list starts or ends
+    exactly at a boundary between two CTA runs of the attention's stream
+    split (32-entry chunks laid end to end, cut into G equal runs, G = the
+    CTAs of one wave: ctas_per_sm per SM), plus the rows on either side."""
+    C = max(1, -(-width // 32))
+    T = R * C
+    lmin = max(-(-(C - 1) // 8), 8)
+    G = max(1, min(sms * ctas_per_sm, T // lmin))
+    rows = set()
+    for b in range(G + 1):
+        x = T * b // G
+        if x % C == 0:
+            r = x // C
+            rows.update(v for v in (r - 1, r) if 0 <= v < R)
+    return sorted(rows)
 
 
 def _pool(cache: torch.Tensor, page_ids, page_halves: int) -> "oracle.PagePool":

@@ -15,7 +15,7 @@ import torch
 
 import sparse_paged_attention_qsa_gb300 as qsa
 from sparse_paged_attention_qsa_gb300 import workloads as W
-from tests._util import oracle_attention, oracle_select
+from tests._util import CORES, oracle_attention, oracle_select, stream_edge_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -81,14 +81,29 @@ def test_attention_config3_premade_lists():
     assert gerr == oerr == 0
 
 
-def test_attention_config4_full_size_sampled_rows():
+def config4_attention_rows(R):
+    """At least 32 rows of the 256-row batch: every row that starts or ends at
+    a boundary of the stream split's runs (and its neighbour), the first and
+    last rows, filled up with every 8th row."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = set(stream_edge_rows(R, 2051, sms)) | {0, 1, R - 2, R - 1}
+    r = 0
+    while len(rows) < 32:
+        rows.add(r)
+        r += 8
+    return sorted(rows)
+
+
+def test_attention_config4_full_size_many_rows():
     w = W.config(4, device=DEV)
     idx = qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, w.cmp_page_table,
                                       w.token_to_request, w.seq_lens, w.query_positions)
     got, gerr = _gpu(w, idx)
     assert gerr == 0
-    rows = [0, 3, 100, 255]
-    exp, _ = oracle_attention(w, idx, rows=rows)
+    rows = config4_attention_rows(w.R)
+    assert len(rows) >= 32
+    exp, oerr = oracle_attention(w, idx, rows=rows, threads=CORES)
+    assert oerr == 0
     assert np.abs(got[rows] - exp).max() <= TOL
     assert np.isfinite(got).all()
 

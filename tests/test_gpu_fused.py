@@ -19,7 +19,7 @@ import torch
 
 import sparse_paged_attention_qsa_gb300 as qsa
 from sparse_paged_attention_qsa_gb300 import workloads as W
-from tests._util import oracle_attention, oracle_select
+from tests._util import CORES, oracle_attention, oracle_select
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,11 +59,20 @@ def test_fused_configs(cfg):
     assert gerr == oerr == 0
 
 
-def test_fused_config4_full_size_sampled_rows():
+def test_fused_config4_full_size_all_rows():
+    # indices of every row bit for bit; attention on at least 32 rows,
+    # including every row at an edge of the stream split's runs
+    from tests.test_gpu_attention import config4_attention_rows
     w = W.config(4, device=DEV)
-    got_idx, got_out, gerr, _ = _check(w, rows=[0, 1, 77, 128, 200, 255])
+    got_idx, got_out, gerr = _fused(w)
     assert gerr == 0
-    assert (got_idx[:, :2048] >= 0).all() and (got_idx[:, 2048:] == -1).all()
+    exp_idx, oerr = oracle_select(w, threads=CORES)
+    assert oerr == 0
+    bad = [r for r in range(w.R) if not np.array_equal(got_idx[r], exp_idx[r])]
+    assert not bad, f"rows differing from the oracle: {bad[:10]}"
+    rows = config4_attention_rows(w.R)
+    exp_out, _ = oracle_attention(w, exp_idx, rows=rows, threads=CORES)
+    assert np.abs(got_out[rows] - exp_out).max() <= TOL
     assert np.isfinite(got_out).all()
 
 

@@ -10,7 +10,7 @@ import torch
 
 import sparse_paged_attention_qsa_gb300 as qsa
 from sparse_paged_attention_qsa_gb300 import workloads as W
-from tests._util import oracle_select
+from tests._util import CORES, oracle_select
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -51,21 +51,19 @@ def test_select_config2_decode_batch():
     assert gerr == oerr == 0
 
 
-def test_select_config4_full_size_sampled_rows():
+def test_select_config4_full_size_all_rows():
+    # the long-context workload (256 rows x 131072 tokens), every row bit for
+    # bit against the oracle (all 65536 compressed pages go to the host)
     w = W.config(4, device=DEV)
     got, gerr = _gpu(w)
     assert gerr == 0
-    rows = [0, 1, 77, 128, 200, 255]
-    exp, _ = oracle_select(w, rows=rows)
-    for i, r in enumerate(rows):
-        assert np.array_equal(got[r], exp[i]), r
-    # every row: 512 blocks -> 2048 distinct tokens in groups of 4; 131072 is a
-    # multiple of 4, so the query token completes the last group and the
-    # tail is empty (columns 2048..2050 stay -1)
+    exp, oerr = oracle_select(w, threads=CORES)
+    assert oerr == 0
+    bad = [r for r in range(w.R) if not np.array_equal(got[r], exp[r])]
+    assert not bad, f"rows differing from the oracle: {bad[:10]}"
+    # 131072 is a multiple of 4, so the query token completes the last group
+    # and the tail is empty (columns 2048..2050 stay -1)
     assert (got[:, :2048] >= 0).all() and (got[:, 2048:] == -1).all()
-    g = got[:, :2048].reshape(256, 512, 4)
-    assert (g[:, :, 0] % 4 == 0).all() and (np.diff(g, axis=2) == 1).all()
-    assert all(len(np.unique(got[r, :2048])) == 2048 for r in range(256))
 
 
 @pytest.mark.parametrize("lens", [[0], [1], [3], [4], [7], [515], [516], [519], [512 + 3, 1027]])
@@ -221,14 +219,14 @@ def test_select_fp8_configs(cfg):
     assert gerr == oerr == 0
 
 
-def test_select_fp8_config4_sampled_rows():
+def test_select_fp8_config4_all_rows():
     w = W.config(4, device=DEV, cmp_dtype="fp8")
     got, gerr = _gpu(w)
     assert gerr == 0
-    rows = [0, 129, 255]
-    exp, _ = oracle_select(w, rows=rows)
-    for i, r in enumerate(rows):
-        assert np.array_equal(got[r], exp[i]), r
+    exp, oerr = oracle_select(w, threads=CORES)
+    assert oerr == 0
+    bad = [r for r in range(w.R) if not np.array_equal(got[r], exp[r])]
+    assert not bad, f"rows differing from the oracle: {bad[:10]}"
     assert (got[:, :2048] >= 0).all() and (got[:, 2048:] == -1).all()
 
 
