@@ -60,7 +60,16 @@ __device__ __forceinline__ int64_t floor_div(int64_t a, int64_t b) {
 // a copy or a phase is bounded by the caller's limit, so a lost completion
 // can never hang the GPU.
 
+#ifdef QSA_WAIT_TEST
+// Test build only (libqsa_waittest.so): waits on a stage give up after 2 ms,
+// so a test that withholds one stage's copy sees the timeout path quickly.
+constexpr uint64_t kWaitLimitNs = 2000000ull;
+#else
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: any longer wait is a fault
+#endif
+// Draining copies already in flight after a timeout always gets the full
+// second: a copy that was issued lands well within it.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -111,12 +120,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
       : "=r"(ok) : "r"(a), "r"(parity) : "memory");
   return ok != 0;
 }
-// Wait for the phase of the given parity; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+// Wait for the phase of the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(a, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

@@ -49,6 +49,9 @@ struct SelectParams {
   int64_t vcap;               // pt_cols * 128
   uint32_t* err;              // nullable
   int R;
+#ifdef QSA_WAIT_TEST
+  int64_t test_withhold;      // test build: CTA 0 issues no copy for this stage fill (-1: none)
+#endif
 };
 
 

@@ -387,6 +387,7 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
   const int64_t w_end = W * (blockIdx.x + 1) / gridDim.x;
   volatile int* abort_flag = &s_abort;
   int64_t issued = 0;
+  int64_t withheld = -1;   // test build: the fill that got no copy (never drained)
 
   if (is_producer_warp) {
     // ---------------- producer (one lane) ----------------
@@ -449,6 +450,14 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
         }
         ++issued;
         if (pg >= 0) {
+#ifdef QSA_WAIT_TEST
+          // test build: leave this fill without a copy, so the consumers'
+          // wait on it runs out (the failure-detection test)
+          if (blockIdx.x == 0 && issued - 1 == p.test_withhold) {
+            withheld = issued - 1;
+            continue;
+          }
+#endif
           mbar_expect_tx(bar_full + 8 * s, kPageBytes);
           tma_load_2d(base + s * kPageBytes, &tmap, 0, pg * KeyCfg<kFp8>::kRowsPerKey * kCmpPageKeys,
                       bar_full + 8 * s, policy);
@@ -513,11 +522,14 @@ score_kernel(const SelectParams p, const __grid_constant__ CUtensorMap tmap) {
     }
   }
   __syncthreads();
-  // After a timeout, let every copy this CTA issued land before it exits.
+  // After a timeout, let every copy this CTA issued land before it exits
+  // (bounded by the full drain limit, whatever the stage waits' limit).
   if (*abort_flag && is_producer_warp && lane == 0) {
     const int64_t first = issued > kStages ? issued - kStages : 0;
     for (int64_t n = first; n < issued; ++n)
-      mbar_wait(bar_full + 8 * (int)(n % kStages), (uint32_t)((n / kStages) & 1));
+      if (n != withheld)
+        mbar_wait(bar_full + 8 * (int)(n % kStages), (uint32_t)((n / kStages) & 1),
+                  kDrainLimitNs);
   }
 }
 
@@ -592,6 +604,13 @@ __device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
 // above(d) < need <= above(d) + hist[d]; returns d and above(d).
 __device__ __forceinline__ void find_digit(TopkShared& sh, uint32_t need, int tid, int lane,
                                            int warp) {
+  // Keys from one score pass always hold such a digit.  If the workspace is
+  // not from one pass (a score kernel whose wait gave up), none may: the
+  // result is then digit 0 with nothing above, so every index stays in range.
+  if (tid == 0) {
+    sh.found_digit = 0;
+    sh.found_above = 0;
+  }
   uint32_t h[kBinsPerThread];
   uint32_t local = 0;
 #pragma unroll
@@ -710,7 +729,10 @@ __device__ __forceinline__ int warp_reserve(int* counter, int cnt, int lane) {
 __device__ __forceinline__ void emit_warp(TopkShared& sh, bool take, uint32_t x, int64_t idx,
                                           int lane) {
   const int slot = warp_slot(&sh.count, take, lane);
-  if (take) sh.keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
+  // at most 512 keys are taken when the keys come from one score pass; the
+  // bound keeps a workspace that does not (after a timeout) inside keys[]
+  if (take && slot < kTopkBlocks)
+    sh.keys[slot] = ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)idx);
 }
 
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
@@ -1095,6 +1117,12 @@ cudaError_t device_info(DeviceInfo** out) {
 
 }  // namespace
 
+#ifdef QSA_WAIT_TEST
+namespace {
+int64_t g_test_withhold = -1;
+}  // namespace
+#endif
+
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
   DeviceInfo* di = nullptr;
@@ -1113,6 +1141,9 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     c.out = p.out + (int64_t)r0 * p.out_stride0;
     c.scores = p.scores + (int64_t)r0 * p.vcap;
     c.umax = p.umax + (int64_t)r0 * (p.vcap / kUnitKeys);
+#ifdef QSA_WAIT_TEST
+    c.test_withhold = r0 == 0 ? g_test_withhold : -1;
+#endif
     const int64_t items = (int64_t)c.R * c.pt_cols;
     const int grid = (int)(items < di->sms ? items : di->sms);
     if (c.key_fp8)
@@ -1147,3 +1178,12 @@ cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a
 }
 
 }  // namespace qsa
+
+#ifdef QSA_WAIT_TEST
+// Test build only, declared in no public header: the next selection launches
+// leave fill `issue` of the score kernel's CTA 0 without a copy (-1: none).
+extern "C" __attribute__((visibility("default"))) void qsa_test_withhold_score_fill(
+    int64_t issue) {
+  qsa::g_test_withhold = issue;
+}
+#endif
