@@ -447,6 +447,9 @@ def run_ours(args, world, rank, local):
     r1 = None
     if not args.no_r1 and args.workload == 4:
         r1 = r1_latency(args, dev, stream)
+    small = None
+    if not args.no_r1 and args.workload == 4:
+        small = small_batches(args, w, dev, stream, peak)
     spec = None
     if not args.no_spec and args.workload == 4:
         spec = spec_variant(args, R, world, rank, dev, stream, peak)
@@ -504,6 +507,7 @@ def run_ours(args, world, rank, local):
         "fp8_compressed_cache": fp8,
         "metadata_builder": meta,
         "latency_R1": r1,
+        "small_batches_L131072": small,
         "speculative_decode": spec,
         "paged_mqa_indexer": indexer,
         "gpu_launches": 4 * K,
@@ -670,6 +674,75 @@ def r1_latency(args, dev, stream):
             res[name] = {"us_median": statistics.median(ts), "us_min": min(ts)}
         out[W.CONFIG_NAMES[cfg]] = res
     return out
+
+
+def small_batches(args, w, dev, stream, peak):
+    """Decode steps of a few rows (the first R rows of the long-context
+    workload, 131072 tokens each) through qsa_select_attend -- one fused
+    kernel for up to 16 rows, the chained kernels above -- and through the
+    two calls.  A 256 MiB buffer is written before every timed call, so
+    each starts with its inputs out of L2; median of 30 calls.  frac = the
+    step's algorithmic bytes at the measured HBM rate / the step's time."""
+    import sparse_paged_attention_qsa_gb300 as qsa
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    seq = w.seq_lens.cpu().numpy()
+    pos = w.query_positions.cpu().numpy()
+    t2r = w.token_to_request.cpu().numpy()
+    cols = w.cmp_page_table.shape[1]
+    res = {}
+    for R in (1, 2, 4, 8, 16, 32, 64):
+        if R > w.R:
+            break
+        x = {n: getattr(w, n)[:R] for n in ("q_sel", "q_attn", "token_to_request",
+                                            "query_positions")}
+        idx = torch.empty((R, 2051), dtype=torch.int32, device=dev)
+        o = torch.empty((R, 3, 256), dtype=torch.float16, device=dev)
+        fws = torch.empty(qsa.qsa_select_attend_workspace_bytes(R, cols), dtype=torch.uint8,
+                          device=dev)
+        sws = torch.empty(qsa.qsa_select_workspace_bytes(R, cols), dtype=torch.uint8,
+                          device=dev)
+        aws = torch.empty(qsa.qsa_attention_workspace_bytes(R, 2051), dtype=torch.uint8,
+                          device=dev)
+
+        def one():
+            qsa.qsa_select_attend(x["q_sel"], w.cmp_cache, w.cmp_page_table,
+                                  x["token_to_request"], w.seq_lens, x["query_positions"],
+                                  x["q_attn"], w.k_view, w.v_view, w.kv_page_table, indices=idx,
+                                  out=o, workspace=fws, stream=stream)
+
+        def two():
+            qsa.qsa_select_paged_tokens(x["q_sel"], w.cmp_cache, w.cmp_page_table,
+                                        x["token_to_request"], w.seq_lens, x["query_positions"],
+                                        out=idx, workspace=sws, stream=stream)
+            qsa.qsa_sparse_attention(x["q_attn"], w.k_view, w.v_view, w.kv_page_table,
+                                     x["token_to_request"], idx, out=o, workspace=aws,
+                                     stream=stream)
+
+        row = {}
+        for name, fn in (("one_call", one), ("two_call", two)):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(30):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            row[name + "_us"] = statistics.median(ts)
+        idx_h = idx.cpu().numpy()
+        nbytes = sum(select_bytes_per_row(int(seq[t2r[r]]), int(pos[r])) +
+                     attend_bytes_per_row(idx_h[r]) for r in range(R))
+        floor_us = nbytes / (peak * 1e9) * 1e6
+        row.update({"rows_per_s": R / (row["one_call_us"] * 1e-6),
+                    "hbm_floor_us": floor_us, "frac_of_floor": floor_us / row["one_call_us"],
+                    "path": ("fused (one cluster per row)" if R <= qsa.qsa_select_attend_fused_rows()
+                             else "chained kernels")})
+        res[f"R{R}"] = row
+    return res
 
 
 def metadata_timing(args, R, world, dev, stream, cmp_pt, seq):

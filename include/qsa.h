@@ -220,8 +220,9 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * attention kernel; "Exact contracts" / Selection and Attention), in one
  * call with one workspace.
  *
- * Results: identical to the two calls on the same inputs -- out_indices bit
- * for bit, out as qsa_sparse_attention over out_indices.
+ * Results: out_indices bit for bit those of qsa_select_paged_tokens; out as
+ * qsa_sparse_attention over out_indices (within its tolerance; bit for bit
+ * too for batches above the fused limit).
  *
  * Arguments: the selection's, as qsa_select_paged_tokens (num_reqs rows in
  * both page tables), then the attention's, as qsa_sparse_attention without
@@ -230,12 +231,17 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * num_rows, cmp_pt_cols) bytes, 256-byte aligned.  out_indices and out must
  * not overlap each other, any input or the workspace.
  *
- * How it runs: the kernels of the two calls on the stream, chained by
- * programmatic dependent launch (score, top-k, attention, merge); nothing
- * waits on the host.  (Running the attention of early rows beside the
- * scoring of later ones was slower at every batch size measured, 17 to 256
- * rows: the scoring needs every SM to reach the HBM rate.)  Calls that
- * share a workspace must not overlap on the GPU.
+ * How it runs: for a batch of at most qsa_select_attend_fused_rows() rows,
+ * one kernel with one thread-block cluster per row -- the cluster's CTAs
+ * score the row's pages, each runs the row's top-512 into its own shared
+ * memory (the index hand-off) and attends over its share of the entries,
+ * and the partials merge through distributed shared memory.  Larger batches
+ * run the kernels of the two calls on the stream, chained by programmatic
+ * dependent launch (score, top-k, attention, merge).  Nothing waits on the
+ * host.  The indices are bit-identical either way; the attention output of
+ * the fused kernel sums the softmax terms in another order than the two
+ * calls' kernels (same tolerance).  Calls that share a workspace must not
+ * overlap on the GPU.
  */
 QSA_API qsa_status qsa_select_attend(
     const void* q_sel, qsa_dtype q_sel_dtype, int64_t num_rows,
@@ -258,6 +264,16 @@ QSA_API qsa_status qsa_select_attend(
     void* out, qsa_dtype out_attn_dtype, const int64_t out_strides[3],
     void* workspace, size_t workspace_bytes,
     uint32_t* error_word, qsa_stream_t stream);
+
+/*
+ * The largest batch qsa_select_attend runs as its fused small-batch kernel
+ * on the current device: as many rows as the device holds clusters of the
+ * kernel at once (8 or 16 CTAs of one SM each), at most 16.  cmp_dtype is
+ * the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3; another tag
+ * gives 0).  0 also when the device runs no such cluster.  The first call
+ * on a device queries its cluster occupancy (host only, nothing launched).
+ */
+QSA_API int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype);
 
 /*
  * qsa_select_paged_tokens_static_scratch -- the same selection, for callers

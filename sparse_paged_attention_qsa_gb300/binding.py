@@ -39,6 +39,7 @@ STATUS = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_DTYPE", 3: "QSA_ERR_SHAPE"
 EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
             "qsa_sparse_attention", "qsa_select_attend_workspace_bytes", "qsa_select_attend",
+            "qsa_select_attend_fused_rows",
             "qsa_static_scratch_bytes",
             "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata",
             "qsa_paged_mqa_logits", "qsa_top_k_per_row_decode")
@@ -135,6 +136,8 @@ def declare_signatures(lib):
         ctypes.c_float,
         vp, ctypes.c_int, p64,
         vp, sz, vp, vp]
+    lib.qsa_select_attend_fused_rows.restype = i64
+    lib.qsa_select_attend_fused_rows.argtypes = [ctypes.c_int]
     lib.qsa_select_attend_workspace_bytes.restype = sz
     lib.qsa_select_attend_workspace_bytes.argtypes = [i64, i64]
     lib.qsa_select_attend.restype = ctypes.c_int
@@ -305,6 +308,12 @@ def qsa_decode(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens, que
 
 def qsa_select_attend_workspace_bytes(num_rows: int, cmp_pt_cols: int) -> int:
     return int(load_library().qsa_select_attend_workspace_bytes(num_rows, cmp_pt_cols))
+
+
+def qsa_select_attend_fused_rows(cmp_dtype=torch.float16) -> int:
+    """The largest batch qsa_select_attend runs as one fused kernel on the
+    current device (include/qsa.h)."""
+    return int(load_library().qsa_select_attend_fused_rows(_DTYPE_TAG.get(cmp_dtype, 0)))
 
 
 def qsa_select_attend(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,

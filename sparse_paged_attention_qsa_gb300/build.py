@@ -9,8 +9,9 @@ statically).  Objects go to ``_build/`` next to this file.
 ``build_wait_test()`` builds ``libqsa_waittest.so``, a test-only variant of
 the selection and attention entry points compiled with QSA_WAIT_TEST: its
 stage waits give up after 2 ms and it exports one extra symbol that makes
-the score kernel's first CTA leave one stage fill without a copy, so the
-failure-detection test can make a device wait run out.  The product library
+the first CTA of the score kernel (or of the fused small-batch kernel) leave
+one stage fill without a copy, so the failure-detection test can make a
+device wait run out.  The product library
 carries neither.
 """
 from __future__ import annotations
@@ -29,7 +30,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa.so")
 WAIT_TEST_LIB = os.path.join(PKG, "libqsa_waittest.so")
-WAIT_TEST_SOURCES = ("qsa_abi.cu", "qsa_select.cu", "qsa_attention.cu")
+WAIT_TEST_SOURCES = ("qsa_abi.cu", "qsa_select.cu", "qsa_attention.cu", "qsa_fused.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]

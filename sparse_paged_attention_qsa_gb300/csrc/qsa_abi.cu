@@ -238,6 +238,11 @@ size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols) 
   return one_call_layout(num_rows, cmp_pt_cols).total;
 }
 
+int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype) {
+  if (cmp_dtype != QSA_DT_F16 && cmp_dtype != QSA_DT_F8E4M3) return 0;
+  return qsa::fused_decode_max_rows(cmp_dtype == QSA_DT_F8E4M3);
+}
+
 size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width) {
   if (num_rows <= 0) return 0;
   return qsa::attention_workspace_bytes(num_rows, index_width < 0 ? 0 : index_width);

@@ -103,5 +103,7 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream);
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream);
 int attention_splits(int64_t R, int64_t width);
+// The largest batch the fused small-batch step takes on the current device.
+int fused_decode_max_rows(bool key_fp8);
 
 }  // namespace qsa

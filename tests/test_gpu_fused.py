@@ -87,6 +87,70 @@ def test_fused_matches_two_call_path():
     assert np.array_equal(got_out, out2.float().cpu().numpy())     # the same kernels
 
 
+# --- batches of up to 16 rows: one fused kernel, one thread-block cluster per
+# row (scoring, top-512 and attention; the index list handed over in shared
+# memory).  Indices bit-exact, attention within the tolerance; the fused
+# attention cuts a row's list differently from the two calls' kernels, so
+# its output is compared with the oracle, not bit for bit with theirs.
+
+@pytest.mark.parametrize("lens", [[131072] * 16, [131072, 519, 9215, 70001, 3, 0, 65536, 4099],
+                                  [2051], [300003, 40003]])
+def test_fused_small_batch_matches_two_calls_and_oracle(lens):
+    w = W.build("small", lens, seed=len(lens) + lens[0] % 97, device=DEV)
+    got_idx, got_out, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+    idx2, out2 = qsa.qsa_decode(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                                w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                                w.kv_page_table)
+    assert np.array_equal(got_idx, idx2.cpu().numpy())
+    assert np.abs(got_out - out2.float().cpu().numpy()).max() <= 2 * TOL
+
+
+@pytest.mark.parametrize("R", [1, 16])
+def test_fused_small_batch_fp8_keys(R):
+    w = W.build("small8", [9215, 131072, 519, 40000][:R] * (R // 4 if R > 4 else 1),
+                cmp_dtype="fp8", distinct_keys=0, seed=70 + R, device=DEV)
+    _, _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
+def test_fused_small_batch_ties_bad_pages_and_requests():
+    w = W.build("smallbad", [6003, 30001, 515, 131072, 2051, 9000], distinct_keys=2,
+                dup_mapping=True, seed=77, device=DEV)
+    pt = w.cmp_page_table.clone()
+    pt[1, 3] = -1                                 # an unmapped compressed page
+    pt[3, 200] = w.cmp_cache.shape[0] + 2         # a page beyond the pool
+    t2r = torch.arange(w.R, dtype=torch.int32, device=DEV)
+    t2r[4] = 99                                   # a row without a request
+    got_idx, got_out, gerr, oerr = _check(w, pt=pt, t2r=t2r)
+    assert gerr == oerr == (qsa.DERR_REQUEST | qsa.DERR_CMP_PAGE)
+    assert (got_idx[4] == -1).all() and (got_out[4] == 0).all()
+
+
+def test_fused_small_batch_bad_kv_pages():
+    w = W.build("smallkv", [9215, 20000, 3000], seed=78, device=DEV)
+    kpt = w.kv_page_table.clone()
+    kpt[0, 3] = -1                                # tokens 1536..2047 of row 0: holes
+    kpt[2, 1] = w.kv_cache.shape[0] + 7
+    w2 = W.Workload(**{**w.__dict__, "kv_page_table": kpt})
+    _, _, gerr, oerr = _check(w2)
+    assert oerr == 0 and gerr == qsa.DERR_KV_PAGE
+
+
+def test_fused_rows_query_and_the_boundary():
+    # the largest batch the fused kernel takes on this GPU (as many rows as
+    # it holds clusters at once), and one row more (the chained kernels)
+    n = qsa.qsa_select_attend_fused_rows()
+    assert 1 <= n <= 16
+    assert qsa.qsa_select_attend_fused_rows(torch.float8_e4m3fn) >= 1
+    assert qsa.qsa_select_attend_fused_rows(torch.float32) == 0
+    cyc = [131072, 9215, 519, 3, 70001, 2052]
+    for R in (n, n + 1):
+        w = W.build("bound", [cyc[i % len(cyc)] for i in range(R)], seed=80 + R, device=DEV)
+        _, _, gerr, oerr = _check(w)
+        assert gerr == oerr == 0
+
+
 def _rows(lens, big):
     """The row list, repeated past 32 rows when the large-batch attention is wanted."""
     return lens * (33 // len(lens) + 1) if big else lens

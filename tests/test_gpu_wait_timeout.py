@@ -6,15 +6,17 @@ stops, lets the copies it issued land, sets QSA_DERR_TIMEOUT in the error
 word and returns, so the context stays usable.  Nothing in a healthy run
 makes such a wait run out, so this test loads libqsa_waittest.so, a build of
 the same sources compiled with QSA_WAIT_TEST: its stage waits give up after
-2 ms, and one extra symbol makes the score kernel's first CTA leave one
-stage fill without a copy (no arrive ever comes for it).  No trap, no bad
-address and no endless loop is involved: the wait ends by its own limit.
+2 ms, and one extra symbol makes the first CTA of the score kernel (or of
+the fused small-batch kernel) leave one stage fill without a copy (no
+arrive ever comes for it).  No trap, no bad address and no endless loop is
+involved: the wait ends by its own limit.
 
 Checks: the call that withholds a fill returns quickly with the timeout bit
 set; the next call on the same stream and workspace is bit-exact again
 (against the product library); the same holds for the one-call step
-qsa_select_attend, whose top-k and attention run over the partial scores
-of the aborted scoring without leaving their buffers.
+qsa_select_attend -- through the fused small-batch kernel and through the
+chained kernels -- whose top-k and attention run over the partial scores of
+the aborted scoring without leaving their buffers.
 """
 import ctypes
 import time
@@ -29,7 +31,7 @@ from sparse_paged_attention_qsa_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-WITHHELD_FILL = 2        # the third page the score kernel's CTA 0 streams
+WITHHELD_FILL = 2        # the third page the first CTA streams
 
 
 def _wait_test_lib():
@@ -40,10 +42,12 @@ def _wait_test_lib():
     return lib
 
 
-def _workload():
-    # 16 rows x 65536 tokens: 2048 compressed pages over the score kernel's
-    # CTAs (one per SM), so CTA 0 streams more than WITHHELD_FILL + 1 pages
-    return W.build("waits", [65536] * 16, seed=51, device=DEV)
+def _workload(rows=16):
+    # rows x 65536 tokens: at 16 rows 2048 compressed pages over the score
+    # kernel's CTAs (one per SM), at 40 rows 5120; either way CTA 0 streams
+    # more than WITHHELD_FILL + 1 pages, as does the first CTA of the fused
+    # small-batch kernel's first cluster (128 pages over 16 or 8 CTAs)
+    return W.build("waits", [65536] * rows, seed=51, device=DEV)
 
 
 def _select(w, lib, ws, err):
@@ -84,9 +88,12 @@ def test_selection_wait_runs_out_then_next_call_is_exact():
                                                    w.query_positions), ref)
 
 
-def test_one_call_step_wait_runs_out_then_next_call_is_exact():
+@pytest.mark.parametrize("rows", [16, 40])
+def test_one_call_step_wait_runs_out_then_next_call_is_exact(rows):
+    # 16 rows: the fused small-batch kernel (one cluster per row); 40 rows:
+    # the chained score, top-k and attention kernels
     lib = _wait_test_lib()
-    w = _workload()
+    w = _workload(rows)
     ref_idx, ref_out = qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table,
                                              w.token_to_request, w.seq_lens, w.query_positions,
                                              w.q_attn, w.k_view, w.v_view, w.kv_page_table)
