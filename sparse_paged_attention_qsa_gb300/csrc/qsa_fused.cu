@@ -51,8 +51,13 @@ constexpr int kFBlockEntries = kTokenTopk;
 constexpr int kFWarpEntries = kFBlockEntries / kFMinCluster / kFWarps;            // <= 16
 static_assert(kFBlockEntries % (kFMaxCluster * kFWarps) == 0, "whole entries per warp");
 static_assert(kFWarpEntries <= 32, "one index load per lane");
+constexpr int kFHelperWarps = kFHelperThreads / 32;   // 7
 constexpr int kFTailWarp = kScoreWarps + 1;   // the helper warp that attends the tail
 constexpr int kStateFloats = 2 + kAttHeads * 8;   // a lane's WarpState
+// Each CTA owns a slice of the row's 3 x 256 outputs; the others push their
+// partials for it into its inbox: per sender, m[3], l[3], acc[slice].
+constexpr int kSliceMax = (kAttHeads * kAttDim + kFMinCluster - 2) / (kFMinCluster - 1);   // 110
+constexpr int kInboxStride = 2 * kAttHeads + kSliceMax;           // floats per sender
 static_assert(kTopkThreads == kFThreads, "the top-k runs on the whole CTA");
 constexpr int kKvPtStaged = 2048;          // K/V page-table entries staged per row
 
@@ -76,13 +81,14 @@ static_assert(sizeof(FusedAttnSmem) <= (size_t)kFRingBytes, "attention fits in t
 constexpr size_t kOffIdx = kFRingBytes;                                   // int32 [2052]
 constexpr size_t kOffQf = kOffIdx + 2052 * 4;                             // QFrag
 constexpr size_t kOffKvPt = kOffQf + sizeof(attn::QFrag);                 // int32 [2048]
-constexpr size_t kOffPart = kOffKvPt + kKvPtStaged * 4;                   // float [774]
-constexpr size_t kOffTail = (kOffPart + attn::kPartFloats * 4 + 15) & ~(size_t)15;   // float [26][32]
-constexpr size_t kOffBars = (kOffTail + kStateFloats * 32 * 4 + 7) & ~(size_t)7;
+constexpr size_t kOffInbox = kOffKvPt + kKvPtStaged * 4;                 // float [16][102]
+constexpr size_t kOffState = kOffInbox + kFMaxCluster * kInboxStride * 4;   // float [7][26][32]
+constexpr size_t kOffHTok = kOffState + kFHelperWarps * kStateFloats * 32 * 4;   // uint32 [7][32]
+constexpr size_t kOffBars = (kOffHTok + kFHelperWarps * 32 * 4 + 7) & ~(size_t)7;
 constexpr size_t kOffCols = kOffBars + 2 * kFMaxStages * 8;               // int [8]
 constexpr size_t kFSmem = 1024 + kOffCols + kFMaxStages * 4;
-static_assert(kOffQf % 16 == 0 && kOffKvPt % 16 == 0 && kOffPart % 16 == 0 &&
-              kOffTail % 16 == 0, "alignment");
+static_assert(kOffQf % 16 == 0 && kOffKvPt % 16 == 0 && kOffInbox % 16 == 0 &&
+              kOffState % 16 == 0 && kOffHTok % 16 == 0, "alignment");
 static_assert(kFSmem <= 227 * 1024, "fused kernel shared memory");
 
 // --- clusters (sm_90+ PTX) ---------------------------------------------------
@@ -107,16 +113,22 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+// The two halves of cluster_sync_all, for a CTA with work of its own between
+// its arrival and the barrier's completion.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // The address of this CTA's shared-memory word `local` in CTA `rank`.
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
+__device__ __forceinline__ void st_dsmem(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 
 // A lane's WarpState to and from shared memory (column `lane` of [26][32]).
@@ -158,6 +170,82 @@ __device__ __forceinline__ int resolve_lane_entries(const AttentionParams& a, in
   return __popc(vmask);
 }
 
+// The CTA's 16 warp states (WarpState layout, in sm) merged into one partial
+// per head and pushed to the owners of the output elements -- the cluster's
+// CTAs f0 .. CS-1, which are also the senders: element o of the row's
+// 3 x 256 goes to CTA f0 + o / per, sender slot c of its inbox; each head's
+// (m, l) goes to every owner.  The merge is the log-sum-exp one
+// (M = max m_w, weights 2^(m_w - M)).  Every thread of the CTA calls this
+// after the warps stored their states; a cluster barrier must follow before
+// an owner reads its inbox.
+__device__ __forceinline__ void merge_push(attn::MergeSmem<kFWarps>& sm, uint32_t inbox, int c,
+                                           int f0, int CS, int tid) {
+  __syncthreads();
+  if (tid < kAttHeads) {   // head tid: the CTA's (m, l), pushed to every owner, and the
+    const int h = tid;     // warps' weights 2^(m_w - M), left in sm.m
+    float M = sm.m[0][h];
+#pragma unroll
+    for (int w = 1; w < kFWarps; ++w) M = fmaxf(M, sm.m[w][h]);
+    float Lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFWarps; ++w) {
+      const float cw = M == -CUDART_INF_F ? 0.f : exp2f(sm.m[w][h] - M);
+      Lsum = fmaf(cw, sm.l[w][h], Lsum);
+      sm.m[w][h] = cw;
+    }
+    for (int q = f0; q < CS; ++q) {
+      st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + h), (uint32_t)q), M);
+      st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + kAttHeads + h), (uint32_t)q), Lsum);
+    }
+  }
+  __syncthreads();
+  const int per = (kAttHeads * kAttDim + (CS - f0) - 1) / (CS - f0);
+  for (int o = tid; o < kAttHeads * kAttDim; o += kFThreads) {
+    const int h = o / kAttDim, d = o % kAttDim;
+    float A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFWarps; ++w) A = fmaf(sm.m[w][h], sm.acc[w][h][d], A);
+    const int q = o / per;
+    st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + 2 * kAttHeads + (o - q * per)),
+                       (uint32_t)(f0 + q)), A);
+  }
+}
+
+// The owner's slice of the row's output: log-sum-exp merge of the senders'
+// (CTAs f0 .. CS-1) partials in its inbox, FP16 round to nearest even.
+__device__ __forceinline__ void owner_write(const AttentionParams& a, int r, const float* inbox,
+                                            int c, int f0, int CS, int tid) {
+  const int per = (kAttHeads * kAttDim + (CS - f0) - 1) / (CS - f0);
+  const int o = (c - f0) * per + tid;
+  if (tid >= per || o >= kAttHeads * kAttDim) return;
+  const int h = o / kAttDim;
+  float M = -CUDART_INF_F;
+  for (int q = f0; q < CS; ++q) M = fmaxf(M, inbox[q * kInboxStride + h]);
+  float A = 0.f, L = 0.f;
+  if (M != -CUDART_INF_F) {
+    for (int q = f0; q < CS; ++q) {
+      const float w = exp2f(inbox[q * kInboxStride + h] - M);
+      L = fmaf(w, inbox[q * kInboxStride + kAttHeads + h], L);
+      A = fmaf(w, inbox[q * kInboxStride + 2 * kAttHeads + tid], A);
+    }
+  }
+  const float inv_l = L > 0.f ? 1.f / L : 0.f;
+  a.out[(int64_t)r * kAttHeads * kAttDim + o] = __float2half_rn(A * inv_l);
+}
+
+// The warp's state into the CTA's merge space (WarpState layout).
+__device__ __forceinline__ void stash_warp(const attn::WarpState& st,
+                                           attn::MergeSmem<kFWarps>& sm, int warp, int lane) {
+#pragma unroll
+  for (int h = 0; h < kAttHeads; ++h)
+#pragma unroll
+    for (int d = 0; d < 8; ++d) sm.acc[warp][h][8 * lane + d] = st.acc[h][d];
+  if (lane < kAttHeads) {
+    sm.m[warp][lane] = st.m_run;
+    sm.l[warp][lane] = st.l_run;
+  }
+}
+
 // topk_row's output: the CTA's shared-memory index list, and out_indices
 // for the cluster's first CTA.
 struct FusedOut {
@@ -186,9 +274,9 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   int32_t* idx_s = reinterpret_cast<int32_t*>(gbase + kOffIdx);
   attn::QFrag& qf = *reinterpret_cast<attn::QFrag*>(gbase + kOffQf);
   int32_t* kvpt_s = reinterpret_cast<int32_t*>(gbase + kOffKvPt);
-  float* part_s = reinterpret_cast<float*>(gbase + kOffPart);
-  float* tail_s = reinterpret_cast<float*>(gbase + kOffTail);
-  uint32_t* ash_tail_tok = reinterpret_cast<uint32_t*>(part_s);   // free until phase C
+  float* inbox_s = reinterpret_cast<float*>(gbase + kOffInbox);
+  float* hstate_s = reinterpret_cast<float*>(gbase + kOffState);
+  uint32_t* htok_s = reinterpret_cast<uint32_t*>(gbase + kOffHTok);
   int* s_col = reinterpret_cast<int*>(gbase + kOffCols);
   const uint32_t bar_full = base + (uint32_t)kOffBars;
   const uint32_t bar_empty = bar_full + kFMaxStages * 8;
@@ -212,6 +300,9 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   const int64_t Vs = rs.ok ? (rs.V < p.vcap ? rs.V : p.vcap) : 0;
   const int npages = (int)((Vs + kCmpPageKeys - 1) / kCmpPageKeys);
   const int nmine = c < npages ? (npages - c + CS - 1) / CS : 0;   // pages c, c + CS, ...
+  // at most 512 scored blocks: the top-512 keeps every block that has a key,
+  // so the attention does not wait for the ranking (the same on every CTA)
+  const bool short_row = Vs <= kTopkBlocks;
   __syncthreads();
   volatile int* abort_flag = &s_abort;
   int issued = 0;
@@ -299,26 +390,46 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
     }
   } else {
     // helpers: the attention's query fragments and the row's K/V page table;
-    // then, in the cluster's last CTA, one warp attends the row's tail tokens
-    // (4V .. tail end: known before the selection)
+    // then attention that needs no ranking: the tail tokens (4V .. tail end,
+    // known before the selection; the cluster's last CTA) and, in a short
+    // row (at most 512 scored blocks, so the top-512 keeps every block whose
+    // page is mapped), the tokens of every such block
     const int ht = tid - (kScoreWarps + 1) * 32;
+    const int hw = warp - (kScoreWarps + 1);
     attn::stage_query(a, r, qf, ht, kFHelperThreads);
     const bool rok = rs.ok && rs.req < a.num_reqs;
     const int64_t ncols = a.pt_cols < kKvPtStaged ? a.pt_cols : kKvPtStaged;
     for (int64_t j = ht; j < ncols; j += kFHelperThreads)
       kvpt_s[j] = rok ? __ldg(a.pt + (int64_t)rs.req * a.pt_stride0 + j) : -1;
     asm volatile("bar.sync 2, %0;" ::"r"(kFHelperThreads) : "memory");   // qf is staged
+    attn::WarpState st;
+    attn::init_state(st);
+    uint32_t* tok = htok_s + 32 * hw;
+    if (short_row && c > 0) {
+      // batch i = blocks 2i, 2i + 1 (tokens 8i .. 8i + 7); helper warp gh of
+      // CTAs 1 .. CS-1 (CTA 0 ranks the row meanwhile) takes batches gh,
+      // gh + (CS - 1) * 7, ...
+      const int nb = (int)((Vs + 1) / 2);
+      for (int i = (c - 1) * kFHelperWarps + hw; i < nb; i += (CS - 1) * kFHelperWarps) {
+        const int64_t b = 2 * (int64_t)i + (lane >> 2);
+        bool keyed = false;
+        if (lane < 8 && b < Vs) {
+          const int32_t pg = __ldg(p.pt + (int64_t)rs.req * p.pt_stride0 + (b >> 7));
+          keyed = pg >= 0 && pg < p.num_pages;
+        }
+        const int32_t iv = keyed ? (int32_t)(8 * i + lane) : -1;
+        const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, -1, tok, lane);
+        attn::attend_tokens_mma(a, tok, n, qf, st, lane);
+      }
+    }
     if (warp == kFTailWarp && c == CS - 1) {
       const int64_t tail0 = rs.V * kRatio;
       const int64_t tail_len = rs.tail_end >= tail0 ? rs.tail_end - tail0 + 1 : 0;
       const int32_t iv = lane < tail_len ? (int32_t)(tail0 + lane) : -1;
-      uint32_t* tok = ash_tail_tok;
-      const int n = resolve_lane_entries(a, rs.req, rok, iv, nullptr, -1, tok, lane);
-      attn::WarpState st;
-      attn::init_state(st);
+      const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, -1, tok, lane);
       attn::attend_tokens_mma(a, tok, n, qf, st, lane);
-      store_state(st, tail_s, lane);
     }
+    store_state(st, hstate_s + kStateFloats * 32 * hw, lane);
   }
   __syncthreads();
   // After a timeout, let every copy this CTA issued land before the ring's
@@ -330,6 +441,35 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   }
   __syncthreads();
   cluster_sync_all();               // every CTA's keys are written and visible
+
+  const uint32_t inbox_a = base + (uint32_t)kOffInbox;
+  if (short_row) {
+    // ---- B'. every entry is attended already.  CTA 0 ranks the row
+    // (out_indices) while CTAs 1 .. CS-1 merge their partials and write the
+    // output; it arrives on the merge's cluster barrier first (it sends and
+    // owns nothing) and waits on it at the end.
+    if (c == 0) {
+      cluster_arrive();
+      const RowOut out{p.out + (int64_t)r * p.out_stride0};
+      if (p.vcap <= kCandCap)
+        topk_row<true>(p, r, tsh, out);
+      else
+        topk_row<false>(p, r, tsh, out);
+      cluster_wait();
+      return;
+    }
+    attn::WarpState st;
+    if (warp > kScoreWarps)
+      load_state(st, hstate_s + kStateFloats * 32 * (warp - kScoreWarps - 1), lane);
+    else
+      attn::init_state(st);
+    attn::finish_mma_state(st, lane);
+    stash_warp(st, ash.merge, warp, lane);
+    merge_push(ash.merge, inbox_a, c, 1, CS, tid);
+    cluster_sync_all();             // every partial is in its owner's inbox
+    owner_write(a, r, inbox_s, c, 1, CS, tid);
+    return;
+  }
 
   // ---- B. the row's top-512, into shared memory --------------------------
   const FusedOut out{idx_s, c == 0 ? p.out + (int64_t)r * p.out_stride0 : nullptr};
@@ -349,49 +489,16 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, rs.V * kRatio, ash.tok[warp],
                                      lane);
   attn::WarpState st;
-  if (warp == kFTailWarp && c == CS - 1)
-    load_state(st, tail_s, lane);
+  if (warp > kScoreWarps)
+    load_state(st, hstate_s + kStateFloats * 32 * (warp - kScoreWarps - 1), lane);
   else
     attn::init_state(st);
   attn::attend_tokens_mma(a, ash.tok[warp], n, qf, st, lane);
   attn::finish_mma_state(st, lane);
-  attn::merge_warps<kFWarps>(st, ash.merge, part_s, tid, warp, lane);
-  cluster_sync_all();               // every CTA's partial is in its shared memory
-
-  // CTA c merges output elements [c*per, (c+1)*per) of the row's 3 x 256
-  const int per = (kAttHeads * kAttDim + CS - 1) / CS;
-  const int o = c * per + tid;
-  if (tid < per && o < kAttHeads * kAttDim) {
-    const int h = o / kAttDim;
-    const uint32_t part_a = base + (uint32_t)kOffPart;
-    float m[kFMaxCluster], l[kFMaxCluster], v[kFMaxCluster];
-#pragma unroll
-    for (int qr = 0; qr < kFMaxCluster; ++qr) {      // every remote load issued first
-      if (qr < CS) {
-        m[qr] = ld_dsmem(dsmem_map(part_a + 4u * h, (uint32_t)qr));
-        l[qr] = ld_dsmem(dsmem_map(part_a + 4u * (kAttHeads + h), (uint32_t)qr));
-        v[qr] = ld_dsmem(dsmem_map(part_a + 4u * (2 * kAttHeads + o), (uint32_t)qr));
-      }
-    }
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int qr = 0; qr < kFMaxCluster; ++qr)
-      if (qr < CS) M = fmaxf(M, m[qr]);
-    float A = 0.f, L = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int qr = 0; qr < kFMaxCluster; ++qr) {
-        if (qr < CS) {
-          const float w = exp2f(m[qr] - M);
-          L = fmaf(w, l[qr], L);
-          A = fmaf(w, v[qr], A);
-        }
-      }
-    }
-    const float inv_l = L > 0.f ? 1.f / L : 0.f;
-    a.out[(int64_t)r * kAttHeads * kAttDim + o] = __float2half_rn(A * inv_l);
-  }
-  cluster_sync_all();               // no CTA leaves while another reads its partial
+  stash_warp(st, ash.merge, warp, lane);
+  merge_push(ash.merge, inbox_a, c, 0, CS, tid);
+  cluster_sync_all();               // every partial is in its owner's inbox
+  owner_write(a, r, inbox_s, c, 0, CS, tid);
 }
 
 template <bool kFp8>

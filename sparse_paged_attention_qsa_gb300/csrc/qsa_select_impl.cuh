@@ -592,8 +592,10 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
              : (ncand < kTopkBlocks ? (uint32_t)ncand : (uint32_t)kTopkBlocks);
   }
   const uint32_t tie_lo = 0x80000000u - (uint32_t)Vs;      // 2^31-1 - (Vs-1)
+  // a row of at most 512 blocks keeps every key: no select, only the ordering
+  const bool all_kept = kDense && Vs <= kTopkThreads;
 
-  if (K > 0) {
+  if (K > 0 && !all_kept) {
     if (fits) {
       // 3. radix select over the candidates
       const Selected sel = radix_select<false, true>(sh, sh.cand_x, ncand, K, lo, M);
@@ -641,6 +643,10 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
   // through shared memory (two buffers, one barrier per step).  Kept keys
   // are distinct and nonzero, so slot i ends with the i-th largest.
   unsigned long long a = tid < (int)K ? sh.keys[tid] : 0ull;
+  if (all_kept) {          // slot tid: block tid's (key, ~index); blocks without a key last
+    const uint32_t x = tid < Vs ? sh.cand_x[tid] : 0u;
+    a = x ? ((unsigned long long)x << 32) | (0xffffffffu - (uint32_t)tid) : 0ull;
+  }
   {
     unsigned long long* const buf0 = sh.keys;
     unsigned long long* const buf1 = reinterpret_cast<unsigned long long*>(sh.cand_x);
