@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic_R256_L131072.json")
 NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e nominal (context; the roofline uses the measured copy rate)
-SELECTION_SOURCES = ("qsa_select.cu", "qsa_device.cuh", "qsa_internal.h")
+SELECTION_SOURCES = ("qsa_select.cu", "qsa_select_impl.cuh", "qsa_device.cuh", "qsa_internal.h")
 
 
 def _selection_traffic(workload: int, rows: int):
@@ -739,7 +739,8 @@ def small_batches(args, w, dev, stream, peak):
         floor_us = nbytes / (peak * 1e9) * 1e6
         row.update({"rows_per_s": R / (row["one_call_us"] * 1e-6),
                     "hbm_floor_us": floor_us, "frac_of_floor": floor_us / row["one_call_us"],
-                    "path": ("fused (one cluster per row)" if R <= qsa.qsa_select_attend_fused_rows()
+                    "path": ("fused (one cluster per row)"
+                             if R <= qsa.qsa_select_attend_fused_rows() and cols <= 128 * R
                              else "chained kernels")})
         res[f"R{R}"] = row
     return res

@@ -231,8 +231,11 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * num_rows, cmp_pt_cols) bytes, 256-byte aligned.  out_indices and out must
  * not overlap each other, any input or the workspace.
  *
- * How it runs: for a batch of at most qsa_select_attend_fused_rows() rows,
- * one kernel with one thread-block cluster per row -- the cluster's CTAs
+ * How it runs: for a batch of at most qsa_select_attend_fused_rows() rows
+ * whose compressed page table has at most 128 columns per row (cmp_pt_cols
+ * <= 128 * num_rows; a wider table means long rows, which the score kernel
+ * spread over every SM scores sooner), one kernel with one thread-block
+ * cluster per row -- the cluster's CTAs
  * score the row's pages, each runs the row's top-512 into its own shared
  * memory (the index hand-off) and attends over its share of the entries,
  * and the partials merge through distributed shared memory.  Larger batches
@@ -268,7 +271,8 @@ QSA_API qsa_status qsa_select_attend(
 /*
  * The largest batch qsa_select_attend runs as its fused small-batch kernel
  * on the current device: as many rows as the device holds clusters of the
- * kernel at once (8 or 16 CTAs of one SM each), at most 16.  cmp_dtype is
+ * kernel at once (8 or 16 CTAs of one SM each), at most 16 (and only when
+ * cmp_pt_cols <= 128 * num_rows, see qsa_select_attend).  cmp_dtype is
  * the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3; another tag
  * gives 0).  0 also when the device runs no such cluster.  The first call
  * on a device queries its cluster occupancy (host only, nothing launched).

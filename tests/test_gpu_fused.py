@@ -139,13 +139,14 @@ def test_fused_small_batch_bad_kv_pages():
 
 def test_fused_rows_query_and_the_boundary():
     # the largest batch the fused kernel takes on this GPU (as many rows as
-    # it holds clusters at once), and one row more (the chained kernels)
+    # it holds clusters at once), and one row more (the chained kernels); a
+    # lone 131072-token row (256 columns) takes the chained kernels too
     n = qsa.qsa_select_attend_fused_rows()
     assert 1 <= n <= 16
     assert qsa.qsa_select_attend_fused_rows(torch.float8_e4m3fn) >= 1
     assert qsa.qsa_select_attend_fused_rows(torch.float32) == 0
     cyc = [131072, 9215, 519, 3, 70001, 2052]
-    for R in (n, n + 1):
+    for R in (1, 2, n, n + 1):
         w = W.build("bound", [cyc[i % len(cyc)] for i in range(R)], seed=80 + R, device=DEV)
         _, _, gerr, oerr = _check(w)
         assert gerr == oerr == 0
