@@ -14,18 +14,24 @@
 //     TMA ring and scores every visible key in the canonical order (the
 //     score kernel's quad code, so the keys are bit-identical), writing the
 //     ordered keys and the unit maxima to the workspace.  Warps 9..15 stage
-//     the attention query and the row's K/V page-table entries meanwhile.
+//     the attention query and the row's K/V page-table entries meanwhile,
+//     and attend what needs no ranking: the tail tokens, and -- in a row of
+//     at most 512 scored blocks, which keeps every block that has a key --
+//     all of the row's tokens.
 //  B. after a cluster barrier every CTA runs the row's exact top-512 (the
 //     top-k kernel's code) into its own shared memory; CTA 0 also writes
-//     out_indices.
-//  C. CTA c attends over its 1/CS of the 2051 entries (16 warps, the
-//     tensor-core walk of the attention kernels), merges its warps into one
-//     partial (m, l, acc) per head; after a cluster barrier it merges its
-//     slice of the output dims over the CS partials, read through
-//     distributed shared memory, and writes FP16.
+//     out_indices.  (A short row is ranked by CTA 0 alone, while the others
+//     go straight to the merge.)
+//  C. CTA c attends over its 2048/CS of the selected blocks' entries (16
+//     warps, the tensor-core walk of the attention kernels), merges its
+//     warps into one partial (m, l, acc) per head and pushes each owner CTA
+//     its slice of the outputs (remote stores into the owner's shared
+//     memory); after a cluster barrier each owner merges its slice over the
+//     senders and writes FP16.
 //
-// Every mbarrier wait is bounded (QSA_DERR_TIMEOUT); the cluster barriers
-// are reached by every thread of every CTA on every path.
+// Every mbarrier wait is bounded (QSA_DERR_TIMEOUT); every cluster barrier
+// is reached by every thread of every CTA of the cluster (the short-row
+// choice is the same on every CTA of a row).
 #include "qsa_internal.h"
 #include "qsa_device.cuh"
 #include "qsa_select_impl.cuh"
