@@ -424,11 +424,12 @@ def qsa_build_metadata(query_start_loc, seq_lens, block_table, num_tokens: int, 
 
 def qsa_paged_mqa_logits(q, kv_cache, weights, context_lens, block_tables, next_n: int,
                          max_model_len: int, *, block_size: int, out=None, error_word=None,
-                         stream=None):
+                         stream=None, library=None):
     """Weighted paged MQA indexer logits (include/qsa_indexer.h): returns fp32
     [rows, max_model_len].  q is E4M3 [rows, heads, 128]; kv_cache holds
-    [num_blocks, block_size*132] bytes (uint8 or float8_e4m3fn storage)."""
-    lib = load_library()
+    [num_blocks, block_size*132] bytes (uint8 or float8_e4m3fn storage).
+    `library` as in qsa_select_paged_tokens."""
+    lib = library or load_library()
     if q.dim() != 3 or kv_cache.dim() != 2 or weights.dim() != 2 or block_tables.dim() != 2:
         raise QSAError(3, "q [rows,H,128], kv_cache [blocks, bs*132], weights [rows,H], "
                           "block_tables 2-D expected")
