@@ -106,10 +106,11 @@ def test_fused_small_batch_matches_two_calls_and_oracle(lens):
     assert np.abs(got_out - out2.float().cpu().numpy()).max() <= 2 * TOL
 
 
-@pytest.mark.parametrize("R", [1, 16])
+@pytest.mark.parametrize("R", [1, 4, 12])
 def test_fused_small_batch_fp8_keys(R):
-    w = W.build("small8", [9215, 131072, 519, 40000][:R] * (R // 4 if R > 4 else 1),
-                cmp_dtype="fp8", distinct_keys=0, seed=70 + R, device=DEV)
+    # 1 and 4 rows: clusters of 16 CTAs; 12 rows: clusters of 8
+    lens = [9215, 131072, 519, 40000] * 3
+    w = W.build("small8", lens[:R], cmp_dtype="fp8", distinct_keys=0, seed=70 + R, device=DEV)
     _, _, gerr, oerr = _check(w)
     assert gerr == oerr == 0
 
@@ -150,6 +151,35 @@ def test_fused_rows_query_and_the_boundary():
         w = W.build("bound", [cyc[i % len(cyc)] for i in range(R)], seed=80 + R, device=DEV)
         _, _, gerr, oerr = _check(w)
         assert gerr == oerr == 0
+
+
+@pytest.mark.parametrize("R", [1, 3, 40])
+def test_fused_empty_compressed_pool(R):
+    # a compressed cache of no pages: every page id is out of range, so no
+    # block has a key -- each row keeps only its tail tokens (fused kernel
+    # for 1 and 3 rows, the chained kernels for 40)
+    lens = [519, 9215, 131072] * (R // 3 + 1)
+    w = W.build("nopool", lens[:R], seed=83 + R, device=DEV)
+    w = W.Workload(**{**w.__dict__, "cmp_cache": w.cmp_cache[:0]})
+    got_idx, got_out, gerr, oerr = _check(w)
+    assert gerr == oerr == qsa.DERR_CMP_PAGE
+    for r, L in enumerate(lens[:R]):
+        tail = list(range(4 * (L // 4), L))
+        assert got_idx[r, :len(tail)].tolist() == tail and (got_idx[r, len(tail):] == -1).all()
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_fused_small_batch_deterministic_on_dirty_workspace(cfg):
+    # the fused kernel (a short row at 519 tokens, a ranked row at 9215):
+    # repeated calls on a dirty workspace give identical indices and outputs
+    w = W.config(cfg, device=DEV)
+    a_idx, a_out, _ = _fused(w)
+    need = qsa.qsa_select_attend_workspace_bytes(w.R, w.cmp_page_table.shape[1])
+    ws = torch.full((need,), 0x5A, dtype=torch.uint8, device=DEV)
+    for _ in range(3):
+        b_idx, b_out, gerr = _fused(w, workspace=ws)
+        assert gerr == 0
+        assert np.array_equal(a_idx, b_idx) and np.array_equal(a_out, b_out)
 
 
 def _rows(lens, big):
