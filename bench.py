@@ -690,6 +690,20 @@ def r1_latency(args, dev, stream):
                 ts.append(a.elapsed_time(b) * 1e3)
             res[name] = {"us_median": statistics.median(ts), "us_min": min(ts)}
         out[W.CONFIG_NAMES[cfg]] = res
+    # the launch floor of this measurement: a one-element kernel timed the
+    # same way (after the flush), for context
+    one = torch.zeros(1, device=dev)
+    ts = []
+    for _ in range(50):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one.add_(1.0)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    out["trivial_kernel_after_flush"] = {"us_median": statistics.median(ts), "us_min": min(ts)}
     return out
 
 
