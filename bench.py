@@ -710,8 +710,8 @@ def r1_latency(args, dev, stream):
 def small_batches(args, w, dev, stream, peak):
     """Decode steps of a few rows (the first R rows of the long-context
     workload, 131072 tokens each) through qsa_select_attend -- one fused
-    kernel for up to 16 rows, the chained kernels above -- and through the
-    two calls.  A 256 MiB buffer is written before every timed call, so
+    kernel while the device holds a cluster per row, the chained kernels
+    above -- and through the two calls.  A 256 MiB buffer is written before every timed call, so
     each starts with its inputs out of L2; median of 30 calls.  frac = the
     step's algorithmic bytes at the measured HBM rate / the step's time."""
     import sparse_paged_attention_qsa_gb300 as qsa
@@ -721,9 +721,10 @@ def small_batches(args, w, dev, stream, peak):
     t2r = w.token_to_request.cpu().numpy()
     cols = w.cmp_page_table.shape[1]
     res = {}
-    for R in (1, 2, 4, 8, 16, 32, 64):
+    for R in (1, 2, 4, 8, 16, 24, 32, 48, 64):
         if R > w.R:
             break
+        cs = qsa.qsa_select_attend_fused_cluster(R, cols)
         x = {n: getattr(w, n)[:R] for n in ("q_sel", "q_attn", "token_to_request",
                                             "query_positions")}
         idx = torch.empty((R, 2051), dtype=torch.int32, device=dev)
@@ -770,8 +771,7 @@ def small_batches(args, w, dev, stream, peak):
         floor_us = nbytes / (peak * 1e9) * 1e6
         row.update({"rows_per_s": R / (row["one_call_us"] * 1e-6),
                     "hbm_floor_us": floor_us, "frac_of_floor": floor_us / row["one_call_us"],
-                    "path": ("fused (one cluster per row)"
-                             if R <= qsa.qsa_select_attend_fused_rows() and cols <= 128 * R
+                    "path": (f"fused (one cluster of {cs} CTAs per row)" if cs
                              else "chained kernels")})
         res[f"R{R}"] = row
     return res

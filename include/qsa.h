@@ -232,10 +232,10 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * not overlap each other, any input or the workspace.
  *
  * How it runs: for a batch of at most qsa_select_attend_fused_rows() rows
- * whose compressed page table has at most 128 columns per row (cmp_pt_cols
- * <= 128 * num_rows; a wider table means long rows, which the score kernel
- * spread over every SM scores sooner), one kernel with one thread-block
- * cluster per row -- the cluster's CTAs
+ * whose compressed page table is narrow enough (qsa_select_attend_fused_
+ * cluster() says; wide tables mean long rows, which the score kernel spread
+ * over every SM scores sooner), one kernel with one thread-block cluster
+ * per row -- the cluster's 4 to 16 CTAs
  * score the row's pages, each runs the row's top-512 into its own shared
  * memory (the index hand-off) and attends over its share of the entries,
  * and the partials merge through distributed shared memory.  Larger batches
@@ -271,13 +271,27 @@ QSA_API qsa_status qsa_select_attend(
 /*
  * The largest batch qsa_select_attend runs as its fused small-batch kernel
  * on the current device: as many rows as the device holds clusters of the
- * kernel at once (8 or 16 CTAs of one SM each), at most 16 (and only when
- * cmp_pt_cols <= 128 * num_rows, see qsa_select_attend).  cmp_dtype is
- * the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3; another tag
- * gives 0).  0 also when the device runs no such cluster.  The first call
- * on a device queries its cluster occupancy (host only, nothing launched).
+ * kernel at once (4 to 16 CTAs of one SM each), at most 64 (and only for
+ * narrow enough page tables, see qsa_select_attend_fused_cluster).
+ * cmp_dtype is the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3;
+ * another tag gives 0).  0 also when the device runs no such cluster.  The
+ * first call on a device queries its cluster occupancy (host only, nothing
+ * launched).
  */
 QSA_API int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype);
+
+/*
+ * How qsa_select_attend runs a batch of num_rows rows whose compressed page
+ * table has cmp_pt_cols columns on the current device: the CTAs of the
+ * fused kernel's cluster per row (4 to 16: the most for which the device
+ * holds num_rows such clusters at once), or 0 for the chained kernels.  The
+ * fused kernel is taken when num_rows <= 64, the device holds num_rows
+ * clusters of at least 4 CTAs, cmp_pt_cols <= 128 * num_rows and every CTA
+ * scores at most 64 pages (ceil(cmp_pt_cols / CTAs) <= 64).  0 for a tag
+ * other than QSA_DT_F16 and QSA_DT_F8E4M3 and for num_rows <= 0.
+ */
+QSA_API int64_t qsa_select_attend_fused_cluster(int64_t num_rows, int64_t cmp_pt_cols,
+                                                qsa_dtype cmp_dtype);
 
 /*
  * qsa_select_paged_tokens_static_scratch -- the same selection, for callers

@@ -9,5 +9,6 @@ from .binding import (  # noqa: F401
     OUT_WIDTH, TOKEN_TOPK, TOPK_BLOCKS, QSAError, declare_signatures, load_library,
     qsa_attention_workspace_bytes,
     qsa_build_metadata, qsa_decode, qsa_paged_mqa_logits, qsa_select_attend,
-    qsa_select_attend_fused_rows, qsa_select_attend_workspace_bytes,
+    qsa_select_attend_fused_rows, qsa_select_attend_fused_cluster,
+    qsa_select_attend_workspace_bytes,
     qsa_top_k_per_row_decode, qsa_select_paged_tokens, qsa_select_workspace_bytes, qsa_sparse_attention)

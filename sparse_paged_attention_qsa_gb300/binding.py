@@ -40,6 +40,7 @@ EXPORTED = ("qsa_status_string", "qsa_version", "qsa_select_workspace_bytes",
             "qsa_select_paged_tokens", "qsa_attention_workspace_bytes",
             "qsa_sparse_attention", "qsa_select_attend_workspace_bytes", "qsa_select_attend",
             "qsa_select_attend_fused_rows",
+            "qsa_select_attend_fused_cluster",
             "qsa_static_scratch_bytes",
             "qsa_select_paged_tokens_static_scratch", "qsa_build_metadata",
             "qsa_paged_mqa_logits", "qsa_top_k_per_row_decode")
@@ -138,6 +139,8 @@ def declare_signatures(lib):
         vp, sz, vp, vp]
     lib.qsa_select_attend_fused_rows.restype = i64
     lib.qsa_select_attend_fused_rows.argtypes = [ctypes.c_int]
+    lib.qsa_select_attend_fused_cluster.restype = i64
+    lib.qsa_select_attend_fused_cluster.argtypes = [i64, i64, ctypes.c_int]
     lib.qsa_select_attend_workspace_bytes.restype = sz
     lib.qsa_select_attend_workspace_bytes.argtypes = [i64, i64]
     lib.qsa_select_attend.restype = ctypes.c_int
@@ -314,6 +317,15 @@ def qsa_select_attend_fused_rows(cmp_dtype=torch.float16) -> int:
     """The largest batch qsa_select_attend runs as one fused kernel on the
     current device (include/qsa.h)."""
     return int(load_library().qsa_select_attend_fused_rows(_DTYPE_TAG.get(cmp_dtype, 0)))
+
+
+def qsa_select_attend_fused_cluster(num_rows: int, cmp_pt_cols: int,
+                                    cmp_dtype=torch.float16) -> int:
+    """CTAs per row's cluster with which qsa_select_attend runs this batch
+    as one fused kernel on the current device, 0 = the chained kernels
+    (include/qsa.h)."""
+    return int(load_library().qsa_select_attend_fused_cluster(
+        num_rows, cmp_pt_cols, _DTYPE_TAG.get(cmp_dtype, 0)))
 
 
 def qsa_select_attend(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,

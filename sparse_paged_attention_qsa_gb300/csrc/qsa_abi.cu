@@ -243,6 +243,13 @@ int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype) {
   return qsa::fused_decode_max_rows(cmp_dtype == QSA_DT_F8E4M3);
 }
 
+int64_t qsa_select_attend_fused_cluster(int64_t num_rows, int64_t cmp_pt_cols,
+                                        qsa_dtype cmp_dtype) {
+  if (cmp_dtype != QSA_DT_F16 && cmp_dtype != QSA_DT_F8E4M3) return 0;
+  if (num_rows <= 0 || num_rows > INT32_MAX) return 0;
+  return qsa::fused_decode_cluster((int)num_rows, cmp_pt_cols, cmp_dtype == QSA_DT_F8E4M3);
+}
+
 size_t qsa_attention_workspace_bytes(int64_t num_rows, int64_t index_width) {
   if (num_rows <= 0) return 0;
   return qsa::attention_workspace_bytes(num_rows, index_width < 0 ? 0 : index_width);

@@ -9,8 +9,8 @@
 // two calls are bound by their launch and dependent-load latencies, not by
 // bytes; here a row's whole step is one cluster's work:
 //
-//  A. scoring -- CTA c of the row's cluster (CS = 16 or 8 CTAs of 512
-//     threads) streams the row's compressed pages c, c + CS, ... through a
+//  A. scoring -- CTA c of the row's cluster (CS = 4 .. 16 CTAs of 512
+//     threads: the most for which the GPU holds a cluster per row) streams the row's compressed pages c, c + CS, ... through a
 //     TMA ring and scores every visible key in the canonical order (the
 //     score kernel's quad code, so the keys are bit-identical), writing the
 //     ordered keys and the unit maxima to the workspace.  Warps 9..15 stage
@@ -48,21 +48,21 @@ constexpr int kFProducerWarp = kScoreWarps;                          // warps 0.
 constexpr int kFHelperThreads = kFThreads - (kScoreWarps + 1) * 32;  // warps 9..15
 constexpr int kFRingBytes = 4 * kCmpPageKeys * kSelDim * 2;          // 128 KiB in flight
 constexpr int kFMaxStages = 8;
-constexpr int kFMinCluster = 8;
+constexpr int kFMinCluster = 4;     // CTAs per row's cluster: 4 .. 16, as many as fit
 constexpr int kFMaxCluster = 16;
 // Phase C covers list positions [0, 2048): the expanded blocks.  The tail
 // tokens (values >= 4V, at most 3, after the blocks) are attended in phase
 // A by one helper warp, so with 16 CTAs every warp walks one 8-token batch.
 constexpr int kFBlockEntries = kTokenTopk;
-constexpr int kFWarpEntries = kFBlockEntries / kFMinCluster / kFWarps;            // <= 16
-static_assert(kFBlockEntries % (kFMaxCluster * kFWarps) == 0, "whole entries per warp");
+constexpr int kFCtaEntriesMax = (kFBlockEntries + kFMinCluster - 1) / kFMinCluster;   // 512
+constexpr int kFWarpEntries = (kFCtaEntriesMax + kFWarps - 1) / kFWarps;            // <= 32
 static_assert(kFWarpEntries <= 32, "one index load per lane");
 constexpr int kFHelperWarps = kFHelperThreads / 32;   // 7
 constexpr int kFTailWarp = kScoreWarps + 1;   // the helper warp that attends the tail
 constexpr int kStateFloats = 2 + kAttHeads * 8;   // a lane's WarpState
 // Each CTA owns a slice of the row's 3 x 256 outputs; the others push their
 // partials for it into its inbox: per sender, m[3], l[3], acc[slice].
-constexpr int kSliceMax = (kAttHeads * kAttDim + kFMinCluster - 2) / (kFMinCluster - 1);   // 110
+constexpr int kSliceMax = (kAttHeads * kAttDim + kFMinCluster - 2) / (kFMinCluster - 1);   // 256
 constexpr int kInboxStride = 2 * kAttHeads + kSliceMax;           // floats per sender
 static_assert(kTopkThreads == kFThreads, "the top-k runs on the whole CTA");
 constexpr int kKvPtStaged = 2048;          // K/V page-table entries staged per row
@@ -486,11 +486,13 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   __syncthreads();                  // the index list is complete
 
   // ---- C. attention over this CTA's share of the blocks' entries ----------
-  const int chunk = kFBlockEntries / CS;
-  const int per_warp = chunk / kFWarps;
+  const int chunk = (kFBlockEntries + CS - 1) / CS;
+  const int per_warp = (chunk + kFWarps - 1) / kFWarps;
+  const int e1 = min(kFBlockEntries, (c + 1) * chunk);
   const int w0 = c * chunk + warp * per_warp;
+  const int w1 = min(e1, w0 + per_warp);
   const bool rok = rs.ok && rs.req < a.num_reqs;
-  const int32_t iv = lane < per_warp ? idx_s[w0 + lane] : -1;
+  const int32_t iv = lane < w1 - w0 ? idx_s[w0 + lane] : -1;
   // the tail (values >= 4V) was attended in phase A
   const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, rs.V * kRatio, ash.tok[warp],
                                      lane);
@@ -532,11 +534,11 @@ cudaLaunchConfig_t fused_config(int R, int cs, cudaStream_t stream, cudaLaunchAt
   return cfg;
 }
 
-// Per device and key type: how many clusters of 16 and of 8 CTAs the GPU
-// holds at once.
+// Per device and key type: how many clusters of cs CTAs the GPU holds at
+// once, cs = kFMinCluster .. kFMaxCluster.
 struct FusedInfo {
   bool ready = false;
-  int max16[2] = {0, 0}, max8[2] = {0, 0};
+  int maxc[2][kFMaxCluster + 1] = {};
 };
 
 cudaError_t fused_info(const FusedInfo** out) {
@@ -552,7 +554,7 @@ cudaError_t fused_info(const FusedInfo** out) {
     if ((e = fused_attrs<false>()) != cudaSuccess) return e;
     if ((e = fused_attrs<true>()) != cudaSuccess) return e;
     for (int f = 0; f < 2; ++f) {
-      for (int cs : {16, 8}) {
+      for (int cs = kFMinCluster; cs <= kFMaxCluster; ++cs) {
         cudaLaunchAttribute attr[1];
         int n = 0;
         cudaLaunchConfig_t cfg = f ? fused_config<true>(1, cs, nullptr, attr)
@@ -563,7 +565,7 @@ cudaError_t fused_info(const FusedInfo** out) {
           cudaGetLastError();
           n = 0;
         }
-        (cs == 16 ? d.max16 : d.max8)[f] = n;
+        d.maxc[f][cs] = n;
       }
     }
     d.ready = true;
@@ -581,27 +583,31 @@ int fused_decode_max_rows(bool key_fp8) {
     return 0;
   }
   const int f = key_fp8 ? 1 : 0;
-  const int n = d->max16[f] > d->max8[f] ? d->max16[f] : d->max8[f];
+  int n = 0;
+  for (int cs = kFMinCluster; cs <= kFMaxCluster; ++cs) n = d->maxc[f][cs] > n ? d->maxc[f][cs] : n;
   return n < kFusedMaxRows ? n : kFusedMaxRows;
 }
 
-int fused_decode_cluster(int R, bool key_fp8) {
+int fused_decode_cluster(int R, int64_t pt_cols, bool key_fp8) {
   if (R <= 0 || R > kFusedMaxRows) return 0;
+  if (pt_cols > (int64_t)kFusedColsPerRow * R) return 0;
   const FusedInfo* d = nullptr;
   if (fused_info(&d) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   const int f = key_fp8 ? 1 : 0;
-  if (d->max16[f] >= R) return 16;
-  if (d->max8[f] >= R) return 8;
+  for (int cs = kFMaxCluster; cs >= kFMinCluster; --cs) {   // the largest cluster that fits
+    if (d->maxc[f][cs] >= R)
+      return (pt_cols + cs - 1) / cs <= kFusedPagesPerCta ? cs : 0;
+  }
   return 0;
 }
 
 cudaError_t launch_fused_decode(const SelectParams& p, const AttentionParams& a,
                                 const CUtensorMap& map, int cs, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
-  if (cs != 16 && cs != 8) return cudaErrorInvalidValue;
+  if (cs < kFMinCluster || cs > kFMaxCluster) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaError_t e;
   if (p.key_fp8) {

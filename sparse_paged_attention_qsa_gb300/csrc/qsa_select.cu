@@ -508,9 +508,7 @@ cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a
   // kernel, and the attention of batches of up to 32 rows of the top-k
   if (p.R == 0) return cudaSuccess;
   cudaError_t e;
-  const int cs = p.pt_cols <= (int64_t)kFusedColsPerRow * p.R
-                     ? fused_decode_cluster(p.R, p.key_fp8 != 0)
-                     : 0;
+  const int cs = fused_decode_cluster(p.R, p.pt_cols, p.key_fp8 != 0);
   if (cs > 0) {   // a few rows: one kernel, one cluster per row
     CUtensorMap map;
     e = encode_cmp_map(p, &map);

@@ -693,17 +693,19 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
 }  // namespace
 
 // The fused small-batch decode step (qsa_fused.cu): one thread-block cluster
-// per row scores, selects and attends in one kernel.
-constexpr int kFusedMaxRows = 16;
-// ... and the compressed page table is at most this many columns wide per
-// row of the batch: one cluster scores a row on 8-16 SMs, so a lone row of
+// per row scores, selects and attends in one kernel.  It takes batches of
+// at most kFusedMaxRows rows (and as many as the device holds clusters of 4
+// or more CTAs at once) ...
+constexpr int kFusedMaxRows = 64;
+// ... whose compressed page table is at most this many columns wide per
+// row of the batch: one cluster scores a row on 4-16 SMs, so a lone row of
 // more pages is scored sooner by the score kernel on every SM (one row of
 // 131072 tokens, 256 columns: 41.6 us fused against 38.6 us chained; two
-// such rows: 40.7 against 42.7).
+// such rows: 40.7 against 42.7) ...
 constexpr int kFusedColsPerRow = 128;
-// CTAs per row's cluster (16 or 8) for R rows, or 0 when the fused step
-// does not apply (more rows, or the device cannot hold R clusters at once).
-int fused_decode_cluster(int R, bool key_fp8);
+// ... and at most this many pages per CTA of the cluster (a CTA scores
+// about 40 GB/s of keys; past this the score kernel on every SM wins).
+constexpr int kFusedPagesPerCta = 64;
 cudaError_t launch_fused_decode(const SelectParams& p, const AttentionParams& a,
                                 const CUtensorMap& map, int cs, cudaStream_t stream);
 

@@ -43,6 +43,13 @@ def test_header_declares_and_library_exports_every_symbol(lib):
     assert {e for e in exported if e.startswith("qsa")} == set(names)
 
 
+def test_package_exports_every_binding_function():
+    from sparse_paged_attention_qsa_gb300 import binding
+    public = {n for n in dir(binding) if n.startswith("qsa_") and callable(getattr(binding, n))}
+    assert public and all(getattr(qsa, n, None) is getattr(binding, n) for n in public), \
+        sorted(n for n in public if not hasattr(qsa, n))
+
+
 def test_header_constants_match_binding():
     src = open(HDR).read()
     consts = dict(re.findall(r"#define\s+(QSA_\w+)\s+(\d+)u?\b", src))

@@ -87,7 +87,7 @@ def test_fused_matches_two_call_path():
     assert np.array_equal(got_out, out2.float().cpu().numpy())     # the same kernels
 
 
-# --- batches of up to 16 rows: one fused kernel, one thread-block cluster per
+# --- small batches: one fused kernel, one thread-block cluster per
 # row (scoring, top-512 and attention; the index list handed over in shared
 # memory).  Indices bit-exact, attention within the tolerance; the fused
 # attention cuts a row's list differently from the two calls' kernels, so
@@ -106,9 +106,10 @@ def test_fused_small_batch_matches_two_calls_and_oracle(lens):
     assert np.abs(got_out - out2.float().cpu().numpy()).max() <= 2 * TOL
 
 
-@pytest.mark.parametrize("R", [1, 4, 12])
+@pytest.mark.parametrize("R", [1, 4, 12, 24])
 def test_fused_small_batch_fp8_keys(R):
-    # 1 and 4 rows: clusters of 16 CTAs; 12 rows: clusters of 8
+    # the device picks the cluster size per batch (on a GB300: 16 CTAs for 1
+    # and 4 rows, fewer for 12 and 24)
     lens = [9215, 131072, 519, 40000] * 3
     w = W.build("small8", lens[:R], cmp_dtype="fp8", distinct_keys=0, seed=70 + R, device=DEV)
     _, _, gerr, oerr = _check(w)
@@ -140,10 +141,11 @@ def test_fused_small_batch_bad_kv_pages():
 
 def test_fused_rows_query_and_the_boundary():
     # the largest batch the fused kernel takes on this GPU (as many rows as
-    # it holds clusters at once), and one row more (the chained kernels); a
-    # lone 131072-token row (256 columns) takes the chained kernels too
+    # it holds clusters of 4 or more CTAs at once), and one row more (the
+    # chained kernels); a lone 131072-token row (256 columns) takes the
+    # chained kernels too
     n = qsa.qsa_select_attend_fused_rows()
-    assert 1 <= n <= 16
+    assert 1 <= n <= 64
     assert qsa.qsa_select_attend_fused_rows(torch.float8_e4m3fn) >= 1
     assert qsa.qsa_select_attend_fused_rows(torch.float32) == 0
     cyc = [131072, 9215, 519, 3, 70001, 2052]
@@ -153,11 +155,51 @@ def test_fused_rows_query_and_the_boundary():
         assert gerr == oerr == 0
 
 
-@pytest.mark.parametrize("R", [1, 3, 40])
+def test_fused_cluster_query():
+    # the cluster size a batch runs with: 4 .. 16 CTAs, never fewer CTAs
+    # for fewer rows; 0 above the fused limit, for tables wider than 128
+    # columns per row or 64 pages per CTA, and for other key types
+    n = qsa.qsa_select_attend_fused_rows()
+    prev = 17
+    for R in range(1, n + 1):
+        cs = qsa.qsa_select_attend_fused_cluster(R, 64)
+        assert 4 <= cs <= 16 and cs <= prev
+        prev = cs
+        assert qsa.qsa_select_attend_fused_cluster(R, 128 * R + 1) == 0
+        assert qsa.qsa_select_attend_fused_cluster(R, 64 * cs + 1) == 0
+        assert qsa.qsa_select_attend_fused_cluster(R, min(128 * R, 64 * cs)) == cs
+    assert qsa.qsa_select_attend_fused_cluster(n + 1, 64) == 0
+    assert qsa.qsa_select_attend_fused_cluster(0, 64) == 0
+    assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float32) == 0
+    assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float8_e4m3fn) >= 4
+
+
+def test_fused_every_cluster_size():
+    # batches of 2 .. n rows of mixed lengths (131072-token rows included:
+    # 256 columns) run with every cluster size the device picks for them;
+    # each is checked against the oracle
+    n = qsa.qsa_select_attend_fused_rows()
+    cyc = [131072, 9215, 519, 70001, 3, 2052, 40000]
+    seen = {}
+    for R in range(2, n + 1):
+        cs = qsa.qsa_select_attend_fused_cluster(R, 256)
+        if cs == 0 or cs in seen:
+            continue
+        seen[cs] = R
+        w = W.build("csize", [cyc[i % len(cyc)] for i in range(R)], seed=90 + R, device=DEV)
+        assert w.cmp_page_table.shape[1] == 256
+        _, _, gerr, oerr = _check(w)
+        assert gerr == oerr == 0, (R, cs)
+    assert len(seen) >= 2, seen
+
+
+@pytest.mark.parametrize("R", [1, 3, "over"])
 def test_fused_empty_compressed_pool(R):
     # a compressed cache of no pages: every page id is out of range, so no
     # block has a key -- each row keeps only its tail tokens (fused kernel
-    # for 1 and 3 rows, the chained kernels for 40)
+    # for 1 and 3 rows, the chained kernels one row above the fused limit)
+    if R == "over":
+        R = qsa.qsa_select_attend_fused_rows() + 1
     lens = [519, 9215, 131072] * (R // 3 + 1)
     w = W.build("nopool", lens[:R], seed=83 + R, device=DEV)
     w = W.Workload(**{**w.__dict__, "cmp_cache": w.cmp_cache[:0]})

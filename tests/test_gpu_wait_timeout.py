@@ -46,7 +46,7 @@ def _workload(rows=16):
     # rows x 65536 tokens: at 16 rows 2048 compressed pages over the score
     # kernel's CTAs (one per SM), at 40 rows 5120; either way CTA 0 streams
     # more than WITHHELD_FILL + 1 pages, as does the first CTA of the fused
-    # small-batch kernel's first cluster (128 pages over 16 or 8 CTAs)
+    # small-batch kernel's first cluster (128 pages over 4 to 16 CTAs)
     return W.build("waits", [65536] * rows, seed=51, device=DEV)
 
 
@@ -88,11 +88,14 @@ def test_selection_wait_runs_out_then_next_call_is_exact():
                                                    w.query_positions), ref)
 
 
-@pytest.mark.parametrize("rows", [16, 40])
+@pytest.mark.parametrize("rows", [16, "over"])
 def test_one_call_step_wait_runs_out_then_next_call_is_exact(rows):
-    # 16 rows: the fused small-batch kernel (one cluster per row); 40 rows:
-    # the chained score, top-k and attention kernels
+    # 16 rows: the fused small-batch kernel (one cluster per row); one row
+    # above its limit: the chained score, top-k and attention kernels
     lib = _wait_test_lib()
+    if rows == "over":
+        rows = qsa.qsa_select_attend_fused_rows() + 1
+    assert (qsa.qsa_select_attend_fused_cluster(rows, 128) > 0) == (rows == 16)
     w = _workload(rows)
     ref_idx, ref_out = qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table,
                                              w.token_to_request, w.seq_lens, w.query_positions,
