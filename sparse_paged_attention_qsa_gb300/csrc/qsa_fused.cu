@@ -9,20 +9,21 @@
 // two calls are bound by their launch and dependent-load latencies, not by
 // bytes; here a row's whole step is one cluster's work:
 //
-//  A. scoring -- CTA c of the row's cluster (CS = 4 .. 16 CTAs of 512
-//     threads: the most for which the GPU holds a cluster per row) streams the row's compressed pages c, c + CS, ... through a
-//     TMA ring and scores every visible key in the canonical order (the
-//     score kernel's quad code, so the keys are bit-identical), writing the
-//     ordered keys and the unit maxima to the workspace.  Warps 9..15 stage
-//     the attention query and the row's K/V page-table entries meanwhile,
-//     and attend what needs no ranking: the tail tokens, and -- in a row of
-//     at most 512 scored blocks, which keeps every block that has a key --
-//     all of the row's tokens.
+//  A. scoring -- CTA c of the row's cluster (CS = 2 .. 16 CTAs of 512
+//     threads: the most for which the GPU holds a cluster per row) streams
+//     the row's compressed pages c, c + CS, ... through a TMA ring and
+//     scores every visible key in the canonical order (the score kernel's
+//     quad code, so the keys are bit-identical), writing the ordered keys
+//     and the unit maxima to the workspace.  Warps 9..15 stage the
+//     attention query and the row's K/V page-table entries meanwhile, and
+//     attend what needs no ranking: the tail tokens, and -- in a row of at
+//     most 512 scored blocks, which keeps every block that has a key, and a
+//     cluster of at least 4 CTAs -- all of the row's tokens.
 //  B. after a cluster barrier every CTA runs the row's exact top-512 (the
 //     top-k kernel's code) into its own shared memory; CTA 0 also writes
 //     out_indices.  (A short row is ranked by CTA 0 alone, while the others
 //     go straight to the merge.)
-//  C. CTA c attends over its 2048/CS of the selected blocks' entries (16
+//  C. CTA c attends over its ceil(2048/CS) of the selected blocks' entries (16
 //     warps, the tensor-core walk of the attention kernels), merges its
 //     warps into one partial (m, l, acc) per head and pushes each owner CTA
 //     its slice of the outputs (remote stores into the owner's shared
@@ -48,23 +49,38 @@ constexpr int kFProducerWarp = kScoreWarps;                          // warps 0.
 constexpr int kFHelperThreads = kFThreads - (kScoreWarps + 1) * 32;  // warps 9..15
 constexpr int kFRingBytes = 4 * kCmpPageKeys * kSelDim * 2;          // 128 KiB in flight
 constexpr int kFMaxStages = 8;
-constexpr int kFMinCluster = 4;     // CTAs per row's cluster: 4 .. 16, as many as fit
+constexpr int kFMinCluster = 2;     // CTAs per row's cluster: 2 .. 16, as many as fit
 constexpr int kFMaxCluster = 16;
+// A short row (at most 512 scored blocks) is attended during the scoring by
+// the helper warps of CTAs 1 .. CS-1 when there are at least this many CTAs;
+// in smaller clusters it takes the ranked path (phase C on every warp).
+constexpr int kFShortRowMinCluster = 4;
 // Phase C covers list positions [0, 2048): the expanded blocks.  The tail
 // tokens (values >= 4V, at most 3, after the blocks) are attended in phase
 // A by one helper warp, so with 16 CTAs every warp walks one 8-token batch.
 constexpr int kFBlockEntries = kTokenTopk;
-constexpr int kFCtaEntriesMax = (kFBlockEntries + kFMinCluster - 1) / kFMinCluster;   // 512
-constexpr int kFWarpEntries = (kFCtaEntriesMax + kFWarps - 1) / kFWarps;            // <= 32
-static_assert(kFWarpEntries <= 32, "one index load per lane");
 constexpr int kFHelperWarps = kFHelperThreads / 32;   // 7
 constexpr int kFTailWarp = kScoreWarps + 1;   // the helper warp that attends the tail
 constexpr int kStateFloats = 2 + kAttHeads * 8;   // a lane's WarpState
-// Each CTA owns a slice of the row's 3 x 256 outputs; the others push their
-// partials for it into its inbox: per sender, m[3], l[3], acc[slice].
-constexpr int kSliceMax = (kAttHeads * kAttDim + kFMinCluster - 2) / (kFMinCluster - 1);   // 256
-constexpr int kInboxStride = 2 * kAttHeads + kSliceMax;           // floats per sender
+// Each owner CTA (f0 .. CS-1; f0 = 1 when CTA 0 ranks a short row alone)
+// holds a slice of `per` of the row's 3 x 256 outputs, and every sender
+// pushes its partial for it into the owner's inbox: m[3], l[3], acc[per]
+// at floats [c * stride, (c + 1) * stride), stride = 6 + per.
+__host__ __device__ constexpr int inbox_slice(int cs, int f0) {
+  return (kAttHeads * kAttDim + (cs - f0) - 1) / (cs - f0);
+}
+constexpr int inbox_floats_max() {
+  int m = 0;
+  for (int cs = kFMinCluster; cs <= kFMaxCluster; ++cs)
+    for (int f0 = 0; f0 <= (cs >= kFShortRowMinCluster ? 1 : 0); ++f0) {
+      const int n = cs * (2 * kAttHeads + inbox_slice(cs, f0));
+      m = n > m ? n : m;
+    }
+  return m;
+}
+constexpr int kInboxFloats = inbox_floats_max();   // 1048 (4 CTAs, short row)
 static_assert(kTopkThreads == kFThreads, "the top-k runs on the whole CTA");
+static_assert(kFShortRowMinCluster >= 2, "a short row needs a merging CTA besides CTA 0");
 constexpr int kKvPtStaged = 2048;          // K/V page-table entries staged per row
 
 template <bool kFp8>
@@ -87,8 +103,8 @@ static_assert(sizeof(FusedAttnSmem) <= (size_t)kFRingBytes, "attention fits in t
 constexpr size_t kOffIdx = kFRingBytes;                                   // int32 [2052]
 constexpr size_t kOffQf = kOffIdx + 2052 * 4;                             // QFrag
 constexpr size_t kOffKvPt = kOffQf + sizeof(attn::QFrag);                 // int32 [2048]
-constexpr size_t kOffInbox = kOffKvPt + kKvPtStaged * 4;                 // float [16][102]
-constexpr size_t kOffState = kOffInbox + kFMaxCluster * kInboxStride * 4;   // float [7][26][32]
+constexpr size_t kOffInbox = kOffKvPt + kKvPtStaged * 4;                 // float [kInboxFloats]
+constexpr size_t kOffState = (kOffInbox + kInboxFloats * 4 + 15) & ~(size_t)15;   // float [7][26][32]
 constexpr size_t kOffHTok = kOffState + kFHelperWarps * kStateFloats * 32 * 4;   // uint32 [7][32]
 constexpr size_t kOffBars = (kOffHTok + kFHelperWarps * 32 * 4 + 7) & ~(size_t)7;
 constexpr size_t kOffCols = kOffBars + 2 * kFMaxStages * 8;               // int [8]
@@ -186,6 +202,8 @@ __device__ __forceinline__ int resolve_lane_entries(const AttentionParams& a, in
 // an owner reads its inbox.
 __device__ __forceinline__ void merge_push(attn::MergeSmem<kFWarps>& sm, uint32_t inbox, int c,
                                            int f0, int CS, int tid) {
+  const int per = inbox_slice(CS, f0);
+  const int stride = 2 * kAttHeads + per;
   __syncthreads();
   if (tid < kAttHeads) {   // head tid: the CTA's (m, l), pushed to every owner, and the
     const int h = tid;     // warps' weights 2^(m_w - M), left in sm.m
@@ -200,19 +218,18 @@ __device__ __forceinline__ void merge_push(attn::MergeSmem<kFWarps>& sm, uint32_
       sm.m[w][h] = cw;
     }
     for (int q = f0; q < CS; ++q) {
-      st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + h), (uint32_t)q), M);
-      st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + kAttHeads + h), (uint32_t)q), Lsum);
+      st_dsmem(dsmem_map(inbox + 4u * (c * stride + h), (uint32_t)q), M);
+      st_dsmem(dsmem_map(inbox + 4u * (c * stride + kAttHeads + h), (uint32_t)q), Lsum);
     }
   }
   __syncthreads();
-  const int per = (kAttHeads * kAttDim + (CS - f0) - 1) / (CS - f0);
   for (int o = tid; o < kAttHeads * kAttDim; o += kFThreads) {
     const int h = o / kAttDim, d = o % kAttDim;
     float A = 0.f;
 #pragma unroll
     for (int w = 0; w < kFWarps; ++w) A = fmaf(sm.m[w][h], sm.acc[w][h][d], A);
     const int q = o / per;
-    st_dsmem(dsmem_map(inbox + 4u * (c * kInboxStride + 2 * kAttHeads + (o - q * per)),
+    st_dsmem(dsmem_map(inbox + 4u * (c * stride + 2 * kAttHeads + (o - q * per)),
                        (uint32_t)(f0 + q)), A);
   }
 }
@@ -221,22 +238,24 @@ __device__ __forceinline__ void merge_push(attn::MergeSmem<kFWarps>& sm, uint32_
 // (CTAs f0 .. CS-1) partials in its inbox, FP16 round to nearest even.
 __device__ __forceinline__ void owner_write(const AttentionParams& a, int r, const float* inbox,
                                             int c, int f0, int CS, int tid) {
-  const int per = (kAttHeads * kAttDim + (CS - f0) - 1) / (CS - f0);
-  const int o = (c - f0) * per + tid;
-  if (tid >= per || o >= kAttHeads * kAttDim) return;
-  const int h = o / kAttDim;
-  float M = -CUDART_INF_F;
-  for (int q = f0; q < CS; ++q) M = fmaxf(M, inbox[q * kInboxStride + h]);
-  float A = 0.f, L = 0.f;
-  if (M != -CUDART_INF_F) {
-    for (int q = f0; q < CS; ++q) {
-      const float w = exp2f(inbox[q * kInboxStride + h] - M);
-      L = fmaf(w, inbox[q * kInboxStride + kAttHeads + h], L);
-      A = fmaf(w, inbox[q * kInboxStride + 2 * kAttHeads + tid], A);
+  const int per = inbox_slice(CS, f0);
+  const int stride = 2 * kAttHeads + per;
+  for (int o = (c - f0) * per + tid, t = tid; t < per && o < kAttHeads * kAttDim;
+       o += kFThreads, t += kFThreads) {
+    const int h = o / kAttDim;
+    float M = -CUDART_INF_F;
+    for (int q = f0; q < CS; ++q) M = fmaxf(M, inbox[q * stride + h]);
+    float A = 0.f, L = 0.f;
+    if (M != -CUDART_INF_F) {
+      for (int q = f0; q < CS; ++q) {
+        const float w = exp2f(inbox[q * stride + h] - M);
+        L = fmaf(w, inbox[q * stride + kAttHeads + h], L);
+        A = fmaf(w, inbox[q * stride + 2 * kAttHeads + t], A);
+      }
     }
+    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+    a.out[(int64_t)r * kAttHeads * kAttDim + o] = __float2half_rn(A * inv_l);
   }
-  const float inv_l = L > 0.f ? 1.f / L : 0.f;
-  a.out[(int64_t)r * kAttHeads * kAttDim + o] = __float2half_rn(A * inv_l);
 }
 
 // The warp's state into the CTA's merge space (WarpState layout).
@@ -308,7 +327,7 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   const int nmine = c < npages ? (npages - c + CS - 1) / CS : 0;   // pages c, c + CS, ...
   // at most 512 scored blocks: the top-512 keeps every block that has a key,
   // so the attention does not wait for the ranking (the same on every CTA)
-  const bool short_row = Vs <= kTopkBlocks;
+  const bool short_row = Vs <= kTopkBlocks && CS >= kFShortRowMinCluster;
   __syncthreads();
   volatile int* abort_flag = &s_abort;
   int issued = 0;
@@ -486,22 +505,27 @@ fused_decode_kernel(const SelectParams p, const AttentionParams a,
   __syncthreads();                  // the index list is complete
 
   // ---- C. attention over this CTA's share of the blocks' entries ----------
+  // CTA c: entries [c * chunk, (c + 1) * chunk), per_warp of them per warp
+  // (8 at CS = 16, 64 at CS = 2), walked 32 at a time
   const int chunk = (kFBlockEntries + CS - 1) / CS;
   const int per_warp = (chunk + kFWarps - 1) / kFWarps;
   const int e1 = min(kFBlockEntries, (c + 1) * chunk);
   const int w0 = c * chunk + warp * per_warp;
   const int w1 = min(e1, w0 + per_warp);
   const bool rok = rs.ok && rs.req < a.num_reqs;
-  const int32_t iv = lane < w1 - w0 ? idx_s[w0 + lane] : -1;
-  // the tail (values >= 4V) was attended in phase A
-  const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, rs.V * kRatio, ash.tok[warp],
-                                     lane);
   attn::WarpState st;
   if (warp > kScoreWarps)
     load_state(st, hstate_s + kStateFloats * 32 * (warp - kScoreWarps - 1), lane);
   else
     attn::init_state(st);
-  attn::attend_tokens_mma(a, ash.tok[warp], n, qf, st, lane);
+  for (int j = w0; j < w1; j += 32) {
+    __syncwarp();                   // the last walk has read tok[]
+    const int32_t iv = lane < w1 - j ? idx_s[j + lane] : -1;
+    // the tail (values >= 4V) was attended in phase A
+    const int n = resolve_lane_entries(a, rs.req, rok, iv, kvpt_s, rs.V * kRatio, ash.tok[warp],
+                                       lane);
+    attn::attend_tokens_mma(a, ash.tok[warp], n, qf, st, lane);
+  }
   attn::finish_mma_state(st, lane);
   stash_warp(st, ash.merge, warp, lane);
   merge_push(ash.merge, inbox_a, c, 0, CS, tid);
@@ -598,8 +622,11 @@ int fused_decode_cluster(int R, int64_t pt_cols, bool key_fp8) {
   }
   const int f = key_fp8 ? 1 : 0;
   for (int cs = kFMaxCluster; cs >= kFMinCluster; --cs) {   // the largest cluster that fits
-    if (d->maxc[f][cs] >= R)
-      return (pt_cols + cs - 1) / cs <= kFusedPagesPerCta ? cs : 0;
+    if (d->maxc[f][cs] >= R) {
+      const int64_t fused = kFusedBaseCost + kFusedPageCost * ((pt_cols + cs - 1) / cs);
+      const int64_t chain = kChainBaseCost + kChainPageCost * R * pt_cols;
+      return fused <= chain ? cs : 0;
+    }
   }
   return 0;
 }

@@ -5,12 +5,14 @@ indices ("vLLM: integrate FP16 packed QSA extension", Summary and "Exact
 contracts"/Selection and Attention; the pages' tie, tail, saturation and
 multi-request cases).
 
-The call runs the two calls' kernels from one workspace, so its outputs
-must equal the two calls' bit for bit.  The attention cuts the index lists
-differently on either side of 32 rows (64-entry splits, or equal runs over
-the batch): the edge cases run both ways (the row list repeated past 32
-rows), and the tests also cover row chunks (more than 1024 rows),
-speculative rows that share a request, and repeated calls on a dirty
+Small batches (as many rows as the GPU holds clusters of the fused kernel,
+at most 64) run one fused kernel; larger ones run the two calls' kernels
+from one workspace, so their outputs must equal the two calls' bit for
+bit.  The edge cases run both ways (the row list repeated past the fused
+limit, which also puts the chained attention past 32 rows, where it cuts
+the index lists into equal runs over the batch), and the tests also cover
+row chunks (more than 1024 rows), speculative rows that share a request,
+every cluster size of the fused kernel, and repeated calls on a dirty
 workspace.  Tolerance as in test_gpu_attention.py.
 """
 import numpy as np
@@ -77,7 +79,10 @@ def test_fused_config4_full_size_all_rows():
 
 
 def test_fused_matches_two_call_path():
-    w = W.config(2, device=DEV)
+    # a batch above the fused kernel's limit: the chained kernels, bit for
+    # bit the two calls' (lengths spread over [512, 65536])
+    n = qsa.qsa_select_attend_fused_rows() + 1
+    w = W.build("chain", [512 + (i * 40503) % 65025 for i in range(n)], seed=1002, device=DEV)
     idx2, out2 = qsa.qsa_decode(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
                                 w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
                                 w.kv_page_table)
@@ -155,23 +160,31 @@ def test_fused_rows_query_and_the_boundary():
         assert gerr == oerr == 0
 
 
+def _fused_wins(R, cols, cs):
+    # include/qsa.h, qsa_select_attend_fused_cluster: 25 us + 0.9 us per page
+    # of a CTA against 50 us + 6.25 ns per page of the batch (x 1600)
+    return 40000 + 1440 * -(-cols // cs) <= 80000 + 10 * R * cols
+
+
 def test_fused_cluster_query():
-    # the cluster size a batch runs with: 4 .. 16 CTAs, never fewer CTAs
+    # the cluster size a batch runs with: 2 .. 16 CTAs, never fewer CTAs
     # for fewer rows; 0 above the fused limit, for tables wider than 128
-    # columns per row or 64 pages per CTA, and for other key types
+    # columns per row, where the chained kernels are estimated faster, and
+    # for other key types
     n = qsa.qsa_select_attend_fused_rows()
     prev = 17
     for R in range(1, n + 1):
-        cs = qsa.qsa_select_attend_fused_cluster(R, 64)
-        assert 4 <= cs <= 16 and cs <= prev
+        cs = qsa.qsa_select_attend_fused_cluster(R, 2)
+        assert 2 <= cs <= 16 and cs <= prev
         prev = cs
-        assert qsa.qsa_select_attend_fused_cluster(R, 128 * R + 1) == 0
-        assert qsa.qsa_select_attend_fused_cluster(R, 64 * cs + 1) == 0
-        assert qsa.qsa_select_attend_fused_cluster(R, min(128 * R, 64 * cs)) == cs
+        for cols in (1, 64, 128, 200, 256, 512, 128 * R, 128 * R + 1):
+            want = cs if cols <= 128 * R and _fused_wins(R, cols, cs) else 0
+            assert qsa.qsa_select_attend_fused_cluster(R, cols) == want, (R, cols)
+    assert qsa.qsa_select_attend_fused_cluster(1, 256) == 0     # a lone row of 131072 tokens
     assert qsa.qsa_select_attend_fused_cluster(n + 1, 64) == 0
     assert qsa.qsa_select_attend_fused_cluster(0, 64) == 0
     assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float32) == 0
-    assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float8_e4m3fn) >= 4
+    assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float8_e4m3fn) >= 2
 
 
 def test_fused_every_cluster_size():
@@ -225,8 +238,10 @@ def test_fused_small_batch_deterministic_on_dirty_workspace(cfg):
 
 
 def _rows(lens, big):
-    """The row list, repeated past 32 rows when the large-batch attention is wanted."""
-    return lens * (33 // len(lens) + 1) if big else lens
+    """The row list, repeated past the fused kernel's limit (and 32 rows) when
+    the chained kernels are wanted."""
+    n = max(qsa.qsa_select_attend_fused_rows(), 32) + 1
+    return lens * (n // len(lens) + 1) if big else lens
 
 
 @pytest.mark.parametrize("big", [False, True])
