@@ -7,6 +7,7 @@
 // GPU.  Only arguments that passed validation reach qsa::launch_*.
 #include "qsa.h"
 #include "qsa_internal.h"
+#include "qsa_fused.h"
 
 #include <algorithm>
 #include <cmath>

@@ -36,6 +36,7 @@
 #include "qsa_internal.h"
 #include "qsa_device.cuh"
 #include "qsa_select_impl.cuh"
+#include "qsa_fused.h"
 #include "qsa_attn_impl.cuh"
 
 #include <mutex>

@@ -103,10 +103,5 @@ cudaError_t launch_attention(const AttentionParams& p, cudaStream_t stream);
 cudaError_t launch_select_attend(const SelectParams& p, const AttentionParams& a,
                                  cudaStream_t stream);
 int attention_splits(int64_t R, int64_t width);
-// The largest batch the fused small-batch step takes on the current device.
-int fused_decode_max_rows(bool key_fp8);
-// CTAs per row's cluster of the fused small-batch kernel for R rows and a
-// compressed page table of pt_cols columns, 0 = the chained kernels.
-int fused_decode_cluster(int R, int64_t pt_cols, bool key_fp8);
 
 }  // namespace qsa

@@ -28,6 +28,7 @@
 #include "qsa_internal.h"
 #include "qsa_device.cuh"
 #include "qsa_select_impl.cuh"
+#include "qsa_fused.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
