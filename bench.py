@@ -535,8 +535,9 @@ def run_ours(args, world, rank, local):
 
 
 def one_call_variant(args, w, R, world, dev, stream, idx, out, err, peak, step_bytes):
-    """One decode step through qsa_select_attend (the two calls' kernels from
-    one call and one workspace), on the same workload and outputs."""
+    """One decode step through qsa_select_attend (one fused kernel for a small
+    batch, else the two calls' kernels from one call and one workspace), on
+    the same workload and outputs."""
     import sparse_paged_attention_qsa_gb300 as qsa
     ws = torch.empty(qsa.qsa_select_attend_workspace_bytes(R, w.cmp_page_table.shape[1]),
                      dtype=torch.uint8, device=dev)
@@ -565,9 +566,11 @@ def one_call_variant(args, w, R, world, dev, stream, idx, out, err, peak, step_b
         raise SystemExit(f"bench.py: device error word {int(err.item())} (one-call path)")
     ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
     gbs = step_bytes / (ms * 1e-3) / 1e9
+    cs = qsa.qsa_select_attend_fused_cluster(R, w.cmp_page_table.shape[1], w.cmp_cache.dtype)
     return {"value": R * world / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms, "steps": K,
             "step_hbm_gbs": gbs, "step_frac_of_peak": gbs / peak,
-            "launches_per_step": 4}
+            "path": f"fused (one cluster of {cs} CTAs per row)" if cs else "chained kernels",
+            "launches_per_step": 1 if cs else 4}
 
 
 def fp8_variant(args, w, R, world, dev, stream, idx, out, att_ws, err, peak):
