@@ -557,26 +557,29 @@ __device__ __forceinline__ void topk_row(const SelectParams& p, int r, TopkShare
     __syncthreads();
     const int nhit = sh.nhit;
     if (nhit <= kBins) {
-      for (int base = 0; base < nhit; base += kTopkThreads) {
-        const int h = base + tid;
+      // four lanes per hit unit, 16 bytes (4 keys) each: one warp load covers
+      // 8 whole units (a lane per unit made every load touch 32 lines; more
+      // loads in flight per thread measured slower)
+      constexpr int kQuadUnits = kTopkThreads / 4;            // units per round
+      const int q = tid & 3;
+      for (int base = 0; base < nhit; base += kQuadUnits) {
+        const int h = base + (tid >> 2);
         const int64_t g = h < nhit ? (int64_t)hit[h] : -1;
-        uint4 v[4];
+        const uint4 v = g >= 0 ? ld_cg16(sc + kUnitKeys * g + 4 * q) : make_uint4(0, 0, 0, 0);
+        const int64_t k0 = kUnitKeys * g + 4 * q;               // this lane's first block
+        uint32_t mask = 0;                                     // bit j: block k0 + j
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          v[j] = g >= 0 ? ld_cg16(sc + kUnitKeys * g + 4 * j) : make_uint4(0, 0, 0, 0);
-        uint32_t mask = 0;                                   // bit j: key j of the unit
-#pragma unroll
-        for (int j = 0; j < kUnitKeys; ++j) {
-          const uint32_t x = g >= 0 && kUnitKeys * g + j < Vs ? u4_at(v[j >> 2], j & 3) : 0u;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t x = g >= 0 && k0 + j < Vs ? u4_at(v, j) : 0u;
           mask |= (uint32_t)(x >= lo) << j;
         }
         int slot = warp_reserve(&sh.ncand, __popc(mask), lane);
 #pragma unroll
-        for (int j = 0; j < kUnitKeys; ++j) {
+        for (int j = 0; j < 4; ++j) {
           if (mask >> j & 1u) {
             if (slot < kCandCap) {
-              sh.cand_x[slot] = u4_at(v[j >> 2], j & 3);
-              sh.cand_i[slot] = (uint32_t)(kUnitKeys * g + j);
+              sh.cand_x[slot] = u4_at(v, j);
+              sh.cand_i[slot] = (uint32_t)(k0 + j);
             }
             ++slot;
           }
