@@ -187,19 +187,22 @@ def test_fused_cluster_query():
     assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float8_e4m3fn) >= 2
 
 
-def test_fused_every_cluster_size():
+@pytest.mark.parametrize("kdt", ["fp16", "fp8"])
+def test_fused_every_cluster_size(kdt):
     # batches of 2 .. n rows of mixed lengths (131072-token rows included:
     # 256 columns) run with every cluster size the device picks for them;
     # each is checked against the oracle
-    n = qsa.qsa_select_attend_fused_rows()
+    tdt = torch.float8_e4m3fn if kdt == "fp8" else torch.float16
+    n = qsa.qsa_select_attend_fused_rows(tdt)
     cyc = [131072, 9215, 519, 70001, 3, 2052, 40000]
     seen = {}
     for R in range(2, n + 1):
-        cs = qsa.qsa_select_attend_fused_cluster(R, 256)
+        cs = qsa.qsa_select_attend_fused_cluster(R, 256, tdt)
         if cs == 0 or cs in seen:
             continue
         seen[cs] = R
-        w = W.build("csize", [cyc[i % len(cyc)] for i in range(R)], seed=90 + R, device=DEV)
+        w = W.build("csize", [cyc[i % len(cyc)] for i in range(R)], cmp_dtype=kdt,
+                    seed=90 + R, device=DEV)
         assert w.cmp_page_table.shape[1] == 256
         _, _, gerr, oerr = _check(w)
         assert gerr == oerr == 0, (R, cs)
