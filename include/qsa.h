@@ -271,7 +271,7 @@ QSA_API qsa_status qsa_select_attend(
 /*
  * The largest batch qsa_select_attend runs as its fused small-batch kernel
  * on the current device: as many rows as the device holds clusters of the
- * kernel at once (2 to 16 CTAs of one SM each), at most 64 (and only for
+ * kernel at once (2 to 16 CTAs of one SM each), at most 128 (and only for
  * narrow enough page tables, see qsa_select_attend_fused_cluster).
  * cmp_dtype is the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3;
  * another tag gives 0).  0 also when the device runs no such cluster.  The
@@ -285,7 +285,7 @@ QSA_API int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype);
  * table has cmp_pt_cols columns on the current device: the CTAs of the
  * fused kernel's cluster per row (2 to 16: the most for which the device
  * holds num_rows such clusters at once), or 0 for the chained kernels.  The
- * fused kernel is taken when num_rows <= 64, the device holds num_rows
+ * fused kernel is taken when num_rows <= 128, the device holds num_rows
  * clusters of at least 2 CTAs, cmp_pt_cols <= 128 * num_rows, and its
  * estimated time is at most the chained kernels': 25 us + 0.9 us per page
  * that one of its CTAs scores (ceil(cmp_pt_cols / CTAs) pages) against

@@ -9,7 +9,7 @@ namespace qsa {
 
 // The step takes batches of at most kFusedMaxRows rows (and as many as the
 // device holds clusters of 2 or more CTAs at once) ...
-constexpr int kFusedMaxRows = 64;
+constexpr int kFusedMaxRows = 128;
 // ... whose compressed page table is at most this many columns wide per
 // row of the batch: one cluster scores a row on 2-16 SMs, so a lone row of
 // more pages is scored sooner by the score kernel on every SM (one row of

@@ -6,7 +6,7 @@ contracts"/Selection and Attention; the pages' tie, tail, saturation and
 multi-request cases).
 
 Small batches (as many rows as the GPU holds clusters of the fused kernel,
-at most 64) run one fused kernel; larger ones run the two calls' kernels
+at most 128) run one fused kernel; larger ones run the two calls' kernels
 from one workspace, so their outputs must equal the two calls' bit for
 bit.  The edge cases run both ways (the row list repeated past the fused
 limit, which also puts the chained attention past 32 rows, where it cuts
@@ -150,7 +150,7 @@ def test_fused_rows_query_and_the_boundary():
     # chained kernels); a lone 131072-token row (256 columns) takes the
     # chained kernels too
     n = qsa.qsa_select_attend_fused_rows()
-    assert 1 <= n <= 64
+    assert 1 <= n <= 128
     assert qsa.qsa_select_attend_fused_rows(torch.float8_e4m3fn) >= 1
     assert qsa.qsa_select_attend_fused_rows(torch.float32) == 0
     cyc = [131072, 9215, 519, 3, 70001, 2052]
