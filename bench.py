@@ -724,7 +724,7 @@ def small_batches(args, w, dev, stream, peak):
     t2r = w.token_to_request.cpu().numpy()
     cols = w.cmp_page_table.shape[1]
     res = {}
-    for R in (1, 2, 4, 8, 16, 24, 32, 40, 48, 56, 64, 72, 76):
+    for R in (1, 2, 4, 8, 16, 24, 32, 40, 48, 56, 64, 72, 76, 96, 128, 144, 152):
         if R > w.R:
             break
         cs = qsa.qsa_select_attend_fused_cluster(R, cols)

@@ -235,7 +235,7 @@ QSA_API size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_p
  * whose compressed page table is narrow enough (qsa_select_attend_fused_
  * cluster() says; wide tables mean long rows, which the score kernel spread
  * over every SM scores sooner), one kernel with one thread-block cluster
- * per row -- the cluster's 2 to 16 CTAs
+ * per row -- the cluster's 1 to 16 CTAs
  * score the row's pages, each runs the row's top-512 into its own shared
  * memory (the index hand-off) and attends over its share of the entries,
  * and the partials merge through distributed shared memory.  Larger batches
@@ -271,7 +271,7 @@ QSA_API qsa_status qsa_select_attend(
 /*
  * The largest batch qsa_select_attend runs as its fused small-batch kernel
  * on the current device: as many rows as the device holds clusters of the
- * kernel at once (2 to 16 CTAs of one SM each), at most 128 (and only for
+ * kernel at once (1 to 16 CTAs of one SM each), at most 256 (and only for
  * narrow enough page tables, see qsa_select_attend_fused_cluster).
  * cmp_dtype is the compressed cache's tag (QSA_DT_F16 or QSA_DT_F8E4M3;
  * another tag gives 0).  0 also when the device runs no such cluster.  The
@@ -283,10 +283,10 @@ QSA_API int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype);
 /*
  * How qsa_select_attend runs a batch of num_rows rows whose compressed page
  * table has cmp_pt_cols columns on the current device: the CTAs of the
- * fused kernel's cluster per row (2 to 16: the most for which the device
+ * fused kernel's cluster per row (1 to 16: the most for which the device
  * holds num_rows such clusters at once), or 0 for the chained kernels.  The
- * fused kernel is taken when num_rows <= 128, the device holds num_rows
- * clusters of at least 2 CTAs, cmp_pt_cols <= 128 * num_rows, and its
+ * fused kernel is taken when num_rows <= 256, the device holds num_rows
+ * clusters of at least one CTA, cmp_pt_cols <= 128 * num_rows, and its
  * estimated time is at most the chained kernels': 25 us + 0.9 us per page
  * that one of its CTAs scores (ceil(cmp_pt_cols / CTAs) pages) against
  * 50 us + 6.25 ns per page of the batch (num_rows * cmp_pt_cols), fits to

@@ -9,7 +9,7 @@
 // two calls are bound by their launch and dependent-load latencies, not by
 // bytes; here a row's whole step is one cluster's work:
 //
-//  A. scoring -- CTA c of the row's cluster (CS = 2 .. 16 CTAs of 512
+//  A. scoring -- CTA c of the row's cluster (CS = 1 .. 16 CTAs of 512
 //     threads: the most for which the GPU holds a cluster per row) streams
 //     the row's compressed pages c, c + CS, ... through a TMA ring and
 //     scores every visible key in the canonical order (the score kernel's
@@ -50,7 +50,7 @@ constexpr int kFProducerWarp = kScoreWarps;                          // warps 0.
 constexpr int kFHelperThreads = kFThreads - (kScoreWarps + 1) * 32;  // warps 9..15
 constexpr int kFRingBytes = 4 * kCmpPageKeys * kSelDim * 2;          // 128 KiB in flight
 constexpr int kFMaxStages = 8;
-constexpr int kFMinCluster = 2;     // CTAs per row's cluster: 2 .. 16, as many as fit
+constexpr int kFMinCluster = 1;     // CTAs per row's cluster: 1 .. 16, as many as fit
 constexpr int kFMaxCluster = 16;
 // A short row (at most 512 scored blocks) is attended during the scoring by
 // the helper warps of CTAs 1 .. CS-1 when there are at least this many CTAs;

@@ -8,10 +8,10 @@
 namespace qsa {
 
 // The step takes batches of at most kFusedMaxRows rows (and as many as the
-// device holds clusters of 2 or more CTAs at once) ...
-constexpr int kFusedMaxRows = 128;
+// device holds clusters of the kernel at once, 1 to 16 CTAs each) ...
+constexpr int kFusedMaxRows = 256;
 // ... whose compressed page table is at most this many columns wide per
-// row of the batch: one cluster scores a row on 2-16 SMs, so a lone row of
+// row of the batch: one cluster scores a row on 1-16 SMs, so a lone row of
 // more pages is scored sooner by the score kernel on every SM (one row of
 // 131072 tokens, 256 columns: 41.6 us fused against 38.6 us chained; two
 // such rows: 40.7 against 42.7) ...
@@ -22,7 +22,8 @@ constexpr int kFusedColsPerRow = 128;
 // of keys), the chained kernels about 50 us + 6.25 ns per page of the batch
 // (R * pt_cols; the score kernel on every SM).  Fits to steps of 1-64 rows
 // of 131072 tokens on a GB300 (fused 39.6-142 us, chained 44-156 us, each
-// within 5 %); in units of 1/1600 us:
+// within 5 %; they also pick the faster path at 72-152 rows); in units of
+// 1/1600 us:
 constexpr int64_t kFusedBaseCost = 40000, kFusedPageCost = 1440;
 constexpr int64_t kChainBaseCost = 80000, kChainPageCost = 10;
 cudaError_t launch_fused_decode(const SelectParams& p, const AttentionParams& a,
