@@ -640,7 +640,9 @@ def r1_latency(args, dev, stream):
     two compressed pages; 9215 tokens, 2303 blocks in a pool of 8192 pages):
     microseconds per call of selection, attention, the two-call step and the
     one-call step.  Before every timed call a 256 MiB buffer is written so
-    the call starts with its inputs out of L2; median and min of 50 calls."""
+    the call starts with its inputs out of L2; median and min of 50 calls.
+    Also per call back to back: 64 steps captured in one CUDA graph (no host
+    work between them; the row's inputs stay in L2), median of 10 replays."""
     import sparse_paged_attention_qsa_gb300 as qsa
     from sparse_paged_attention_qsa_gb300 import workloads as W
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -656,25 +658,25 @@ def r1_latency(args, dev, stream):
         fws = torch.empty(qsa.qsa_select_attend_workspace_bytes(1, cols), dtype=torch.uint8,
                           device=dev)
 
-        def sel():
+        def sel(s=stream):
             qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, w.cmp_page_table,
                                         w.token_to_request, w.seq_lens, w.query_positions,
-                                        out=idx, workspace=sws, stream=stream)
+                                        out=idx, workspace=sws, stream=s)
 
-        def att():
+        def att(s=stream):
             qsa.qsa_sparse_attention(w.q_attn, w.k_view, w.v_view, w.kv_page_table,
                                      w.token_to_request, idx, out=o, workspace=aws,
-                                     stream=stream)
+                                     stream=s)
 
-        def both():
-            sel()
-            att()
+        def both(s=stream):
+            sel(s)
+            att(s)
 
-        def fused():
+        def fused(s=stream):
             qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
                                   w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
                                   w.kv_page_table, indices=idx, out=o, workspace=fws,
-                                  stream=stream)
+                                  stream=s)
 
         res = {}
         for name, fn in (("select", sel), ("attend", att), ("two_call_step", both),
@@ -692,6 +694,29 @@ def r1_latency(args, dev, stream):
                 b.synchronize()
                 ts.append(a.elapsed_time(b) * 1e3)
             res[name] = {"us_median": statistics.median(ts), "us_min": min(ts)}
+        side = torch.cuda.Stream(dev)
+        for name, fn in (("two_call_step", both), ("one_call_step", fused)):
+            g = torch.cuda.CUDAGraph()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                fn(side)
+                side.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(64):
+                        fn(side)
+            stream.wait_stream(side)
+            g.replay()
+            ts = []
+            for _ in range(10):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3 / 64)
+            res[name]["back_to_back_us"] = statistics.median(ts)
+            del g
         out[W.CONFIG_NAMES[cfg]] = res
     # the launch floor of this measurement: a one-element kernel timed the
     # same way (after the flush), for context
