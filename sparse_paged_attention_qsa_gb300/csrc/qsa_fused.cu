@@ -1,13 +1,15 @@
-// qsa_fused.cu -- the one-call decode step for small batches on sm_103a: one
-// kernel, one thread-block cluster per row, the selected index list handed
-// from the top-k to the attention in shared memory.
+// qsa_fused.cu -- the one-call decode step for batches that fit in one wave
+// on sm_103a: one kernel, one thread-block cluster per row, the selected
+// index list handed from the top-k to the attention in shared memory.
 //
 // "vLLM: integrate FP16 packed QSA extension", Summary (fused selection and
 // the exact-packed attention kernel) and "Exact contracts"/Selection and
 // Attention; the decode rows of qsa_cache.py (_logical_positions,
 // _build_qsa_metadata_kernel).  For a few rows the chained kernels of the
 // two calls are bound by their launch and dependent-load latencies, not by
-// bytes; here a row's whole step is one cluster's work:
+// bytes, and up to a wave of rows their stages do not overlap; here a row's
+// whole step is one cluster's work, every row's cluster resident at once
+// (which batches take it: qsa_fused.h):
 //
 //  A. scoring -- CTA c of the row's cluster (CS = 1 .. 16 CTAs of 512
 //     threads: the most for which the GPU holds a cluster per row) streams
@@ -24,7 +26,8 @@
 //     out_indices.  (A short row is ranked by CTA 0 alone, while the others
 //     go straight to the merge.)
 //  C. CTA c attends over its ceil(2048/CS) of the selected blocks' entries (16
-//     warps, the tensor-core walk of the attention kernels), merges its
+//     warps, 8 to 128 entries each, walked 32 at a time with the tensor-core
+//     walk of the attention kernels), merges its
 //     warps into one partial (m, l, acc) per head and pushes each owner CTA
 //     its slice of the outputs (remote stores into the owner's shared
 //     memory); after a cluster barrier each owner merges its slice over the
