@@ -312,3 +312,25 @@ def test_top_k_per_row_fails_closed(lib, over, status):
 
 def test_top_k_per_row_nothing_to_do(lib):
     assert _topk(lib, rows=0, batch=0) == 0
+
+
+def test_fused_cost_fit_constants_agree():
+    # the fused-or-chained rule in csrc/qsa_fused.h, the figures include/qsa.h
+    # states for it, and the copy of the rule the GPU tests check the
+    # library's choice against must stay one rule
+    from tests import test_gpu_fused as tf
+    src = open(os.path.join(os.path.dirname(INC), "sparse_paged_attention_qsa_gb300", "csrc",
+                            "qsa_fused.h")).read()
+    c = {k: int(v) for k, v in re.findall(r"(k(?:Fused|Chain)\w+Cost) = (\d+)", src)}
+    assert c == {"kFusedBaseCost": 40000, "kFusedPageCost": 1440, "kChainBaseCost": 80000,
+                 "kChainPageCost": 10}
+    # in microseconds: 25 + 0.9 per page of a CTA against 50 + 0.00625 per page of the batch
+    assert (c["kFusedBaseCost"] / 1600, c["kFusedPageCost"] / 1600) == (25.0, 0.9)
+    assert (c["kChainBaseCost"] / 1600, c["kChainPageCost"] / 1600) == (50.0, 0.00625)
+    hdr = open(HDR).read()
+    assert "25 us + 0.9 us per page" in hdr and "50 us + 6.25 ns per page" in hdr
+    for R, cols, cs in ((1, 2, 16), (32, 256, 4), (48, 256, 2), (64, 256, 2), (100, 256, 1),
+                        (152, 256, 1)):
+        fused = c["kFusedBaseCost"] + c["kFusedPageCost"] * -(-cols // cs)
+        chain = c["kChainBaseCost"] + c["kChainPageCost"] * R * cols
+        assert tf._fused_wins(R, cols, cs) == (fused <= chain)
