@@ -160,6 +160,54 @@ def test_static_scratch_validates_before_the_size_check(lib, over, status):
     assert _static_sel(lib, **over) == status
 
 
+# --- fail-closed one-call step ---------------------------------------------
+
+def _sa(lib, **over):
+    """qsa_select_attend: the selection's and the attention's arguments."""
+    R = over.pop("R", 4)
+    cols = over.pop("cols", 8)
+    k = over.pop("k", _addr(10))
+    a = dict(q=_addr(1), qdt=1, R=R, qs=_arr([512, 128, 1]),
+             cmp=_addr(2), cdt=1, cshape=_arr([64, 128, 1, 128]), cstr=_arr([16384, 128, 128, 1]),
+             pt=_addr(40), ptdt=4, nreq=R, cols=cols, pts0=cols,
+             t2r=_addr(50), t2rdt=4, sl=_addr(60), sldt=4, qp=_addr(70), qpdt=5,
+             topk=2048, ratio=4, idx=_addr(80), idt=4, ow=2051, os0=2051,
+             qa=_addr(90), qadt=1, qas=_arr([768, 256, 1]),
+             k=k, v=over.pop("v", None if k is None else k + 512), kvdt=1,
+             kvshape=_arr([64, 512, 1, 256]), ks=_arr([262144, 512, 256, 1]),
+             vs=_arr([262144, 512, 256, 1]),
+             kvpt=_addr(500), kvptdt=4, kvcols=16, kvpts0=16, scale=1.0 / 16.0,
+             out=_addr(600), odt=1, os=_arr([768, 256, 1]),
+             ws=_addr(700), wsb=lib.qsa_select_attend_workspace_bytes(R, cols), err=None,
+             stream=None)
+    a.update(over)
+    return lib.qsa_select_attend(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qdt=3), 2), (dict(cdt=2), 2), (dict(qadt=3), 2), (dict(kvdt=2), 2), (dict(odt=3), 2),
+    (dict(kvptdt=5), 2), (dict(idt=5), 2),
+    (dict(topk=1024), 6), (dict(scale=float("nan")), 6), (dict(scale=0.0), 6),
+    (dict(R=70000), 3), (dict(kvshape=_arr([64, 256, 1, 256])), 3),
+    (dict(cshape=_arr([64, 64, 1, 128])), 3),
+    (dict(qas=_arr([768, 1, 3])), 4), (dict(kvpts0=8), 4), (dict(pts0=4), 4),
+    (dict(qa=None), 1), (dict(k=None, v=None), 1), (dict(kvpt=None), 1), (dict(out=None), 1),
+    (dict(idx=None), 1),
+    (dict(qa=_addr(90) + 2), 5), (dict(out=_addr(600) + 8), 5), (dict(ws=_addr(700) + 16), 5),
+    (dict(ws=None), 7), (dict(wsb=16), 7),
+    (dict(out=_addr(80)), 8), (dict(out=_addr(700)), 8), (dict(idx=_addr(1)), 8),
+    (dict(idx=_addr(700)), 8), (dict(err=_addr(600)), 8), (dict(err=_addr(80)), 8),
+])
+def test_select_attend_fails_closed(lib, over, status):
+    # every rejection comes from the host checks, before any launch
+    assert _sa(lib, **over) == status
+
+
+def test_select_attend_zero_rows_is_noop(lib):
+    assert lib.qsa_select_attend_workspace_bytes(0, 8) == 0
+    assert _sa(lib, R=0, ws=None, wsb=0) == 0
+
+
 # --- fail-closed attention --------------------------------------------------
 
 def _att(lib, **over):
