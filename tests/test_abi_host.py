@@ -203,6 +203,18 @@ def test_select_attend_fails_closed(lib, over, status):
     assert _sa(lib, **over) == status
 
 
+def test_fused_path_queries_without_a_device_answer(lib):
+    # the answers that need no device: other key types, empty batches, more
+    # rows than the kernel takes, tables wider than 128 columns per row
+    assert lib.qsa_select_attend_fused_rows(4) == 0          # int32 tag
+    assert lib.qsa_select_attend_fused_cluster(1, 2, 4) == 0
+    assert lib.qsa_select_attend_fused_cluster(0, 2, 1) == 0
+    assert lib.qsa_select_attend_fused_cluster(-3, 2, 1) == 0
+    assert lib.qsa_select_attend_fused_cluster(257, 2, 1) == 0
+    assert lib.qsa_select_attend_fused_cluster(2, 257, 1) == 0
+    assert lib.qsa_select_attend_fused_cluster(1 << 40, 2, 1) == 0
+
+
 def test_select_attend_zero_rows_is_noop(lib):
     assert lib.qsa_select_attend_workspace_bytes(0, 8) == 0
     assert _sa(lib, R=0, ws=None, wsb=0) == 0
