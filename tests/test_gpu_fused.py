@@ -187,6 +187,17 @@ def test_fused_cluster_query():
     assert qsa.qsa_select_attend_fused_cluster(1, 2, torch.float8_e4m3fn) >= 2
 
 
+@pytest.mark.parametrize("cols", [256, 257])
+def test_fused_page_table_width_boundary(cols):
+    # two rows of 131072 tokens: a table of 128 columns per row takes the
+    # fused kernel, one column more (unused, -1) the chained kernels; both
+    # match the oracle
+    w = W.build("width", [131072, 9215], cmp_cols=cols, seed=95, device=DEV)
+    assert (qsa.qsa_select_attend_fused_cluster(2, cols) > 0) == (cols == 256)
+    _, _, gerr, oerr = _check(w)
+    assert gerr == oerr == 0
+
+
 @pytest.mark.parametrize("kdt", ["fp16", "fp8"])
 def test_fused_every_cluster_size(kdt):
     # batches of 2 .. n rows of mixed lengths (131072-token rows included:
