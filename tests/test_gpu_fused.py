@@ -372,3 +372,67 @@ def test_fused_fails_closed():
                               w.kv_page_table, indices=idx,
                               out=idx.view(torch.float16).as_strided((1, 3, 256), (768, 256, 1)))
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("rows", [1, 8, "over"])
+def test_steps_captured_in_a_cuda_graph(rows):
+    # serving loops capture the decode step in a CUDA graph: the one-call
+    # step (the fused kernel for 1 and 8 rows, the chained kernels above the
+    # fused limit) and the two calls replay bit for bit like eager calls,
+    # on new inputs copied into the captured buffers
+    if rows == "over":
+        rows = qsa.qsa_select_attend_fused_rows() + 1
+    lens = [9215, 131072, 519, 40000] * (rows // 4 + 1)
+    w = W.build("graph", lens[:rows], seed=97, device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(98)
+    new_q = (torch.randn(w.q_sel.shape, generator=gen, device=DEV).half(),
+             torch.randn(w.q_attn.shape, generator=gen, device=DEV).half())
+    R, cols = w.R, w.cmp_page_table.shape[1]
+    idx = torch.empty((R, 2051), dtype=torch.int32, device=DEV)
+    out = torch.empty((R, 3, 256), dtype=torch.float16, device=DEV)
+    ws = torch.empty(qsa.qsa_select_attend_workspace_bytes(R, cols), dtype=torch.uint8,
+                     device=DEV)
+    idx2 = torch.empty_like(idx)
+    out2 = torch.empty_like(out)
+    sws = torch.empty(qsa.qsa_select_workspace_bytes(R, cols), dtype=torch.uint8, device=DEV)
+    aws = torch.empty(qsa.qsa_attention_workspace_bytes(R, 2051), dtype=torch.uint8, device=DEV)
+    q_sel, q_attn = w.q_sel.clone(), w.q_attn.clone()
+    side = torch.cuda.Stream()
+
+    def one(s):
+        qsa.qsa_select_attend(q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                              w.seq_lens, w.query_positions, q_attn, w.k_view, w.v_view,
+                              w.kv_page_table, indices=idx, out=out, workspace=ws, stream=s)
+
+    def two(s):
+        qsa.qsa_select_paged_tokens(q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                                    w.seq_lens, w.query_positions, out=idx2, workspace=sws,
+                                    stream=s)
+        qsa.qsa_sparse_attention(q_attn, w.k_view, w.v_view, w.kv_page_table,
+                                 w.token_to_request, idx2, out=out2, workspace=aws, stream=s)
+
+    graphs = []
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        one(side)
+        two(side)
+        side.synchronize()
+        for fn in (one, two):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                fn(side)
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(side)
+    for q_s, q_a in ((w.q_sel, w.q_attn), new_q):
+        q_sel.copy_(q_s)
+        q_attn.copy_(q_a)
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        got = (idx.clone(), out.clone(), idx2.clone(), out2.clone())
+        one(torch.cuda.current_stream())
+        two(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], idx) and torch.equal(got[1], out)
+        assert torch.equal(got[2], idx2) and torch.equal(got[3], out2)
+        assert torch.equal(idx, idx2)
