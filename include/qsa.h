@@ -32,6 +32,10 @@
  *     count as absent (a hole) and ORs a QSA_DERR_* bit into *error_word when
  *     error_word is not NULL.  Kernels never trap.
  *   - Concurrent calls that share a workspace race; give each stream its own.
+ *   - Any host thread may call.  The work runs on the calling thread's current
+ *     device (cudaGetDevice), to which the call binds the thread's CUDA
+ *     context before it launches; the stream and every pointer must belong
+ *     to that device.
  *   - FP16 tensors must start on a 16-byte boundary; int tensors on their
  *     element size.  num_rows == 0 is a legal no-op.
  */

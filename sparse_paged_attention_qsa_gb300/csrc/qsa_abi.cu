@@ -8,6 +8,7 @@
 #include "qsa.h"
 #include "qsa_internal.h"
 #include "qsa_fused.h"
+#include "qsa_host.h"
 
 #include <algorithm>
 #include <cmath>
@@ -241,6 +242,7 @@ size_t qsa_select_attend_workspace_bytes(int64_t num_rows, int64_t cmp_pt_cols) 
 
 int64_t qsa_select_attend_fused_rows(qsa_dtype cmp_dtype) {
   if (cmp_dtype != QSA_DT_F16 && cmp_dtype != QSA_DT_F8E4M3) return 0;
+  qsa::bind_calling_thread();
   return qsa::fused_decode_max_rows(cmp_dtype == QSA_DT_F8E4M3);
 }
 
@@ -248,6 +250,7 @@ int64_t qsa_select_attend_fused_cluster(int64_t num_rows, int64_t cmp_pt_cols,
                                         qsa_dtype cmp_dtype) {
   if (cmp_dtype != QSA_DT_F16 && cmp_dtype != QSA_DT_F8E4M3) return 0;
   if (num_rows <= 0 || num_rows > INT32_MAX) return 0;
+  qsa::bind_calling_thread();
   return qsa::fused_decode_cluster((int)num_rows, cmp_pt_cols, cmp_dtype == QSA_DT_F8E4M3);
 }
 
@@ -294,6 +297,7 @@ qsa_status qsa_select_paged_tokens(
   if (error_word && overlaps(span(error_word, 4), ws)) return QSA_ERR_ALIAS;
   p.scores = static_cast<uint32_t*>(workspace);
   p.umax = p.scores + num_rows * p.vcap;
+  qsa::bind_calling_thread();
   const cudaError_t e = qsa::launch_select(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
@@ -331,6 +335,7 @@ qsa_status qsa_sparse_attention(
   }
   p.part = static_cast<float*>(workspace);
   p.nsplit = qsa::attention_splits(num_rows, index_width);
+  qsa::bind_calling_thread();
   const cudaError_t e = qsa::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
@@ -394,6 +399,7 @@ qsa_status qsa_select_attend(
   p.scores = reinterpret_cast<uint32_t*>(w);
   p.umax = p.scores + num_rows * p.vcap;
   a.part = reinterpret_cast<float*>(w + l.part);
+  qsa::bind_calling_thread();
   const cudaError_t e = qsa::launch_select_attend(p, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

@@ -46,6 +46,7 @@
 #include "qsa.h"
 #include "qsa_indexer.h"
 #include "qsa_device.cuh"
+#include "qsa_host.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -1147,6 +1148,7 @@ extern "C" qsa_status qsa_paged_mqa_logits(
   if (error_word && (overlaps(span(error_word, 4), out))) return QSA_ERR_ALIAS;
 
   DevInfo* di = nullptr;
+  bind_calling_thread();
   if (dev_info(&di) != cudaSuccess) return QSA_ERR_CUDA;
   auto fn = encode_fn();
   if (!fn) return QSA_ERR_CUDA;
@@ -1243,6 +1245,7 @@ extern "C" qsa_status qsa_top_k_per_row_decode(
   if (overlaps(out, span(logits, lg_extent)) || overlaps(out, span(seq_lens, batch * 4)))
     return QSA_ERR_ALIAS;
   DevInfo* di = nullptr;
+  bind_calling_thread();
   if (dev_info(&di) != cudaSuccess) return QSA_ERR_CUDA;
   TkParams p{};
   p.logits = static_cast<const float*>(logits);

@@ -19,6 +19,7 @@
 #include "qsa.h"
 #include "qsa_metadata.h"
 #include "qsa_device.cuh"
+#include "qsa_host.h"
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -266,6 +267,7 @@ extern "C" qsa_status qsa_build_metadata(
   p.work = max_num_work > 0 ? work_metadata : nullptr;
   p.max_work = (int)max_num_work;
   const int64_t grid = (units + kMetaThreads - 1) / kMetaThreads;
+  qsa::bind_calling_thread();
   metadata_kernel<<<(unsigned)grid, kMetaThreads, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

@@ -36,6 +36,7 @@
 // an earlier call wrote; the indices of that call are undefined.
 #include "qsa.h"
 #include "qsa_internal.h"
+#include "qsa_host.h"
 
 namespace {
 
@@ -70,6 +71,7 @@ qsa_status qsa_select_paged_tokens_static_scratch(
   if (qsa::select_workspace_bytes(num_rows, cmp_pt_cols) > kStaticScratchBytes)
     return QSA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
+  qsa::bind_calling_thread();
   if (cudaGetSymbolAddress(&scratch, g_select_scratch) != cudaSuccess || scratch == nullptr)
     return QSA_ERR_CUDA;
   return qsa_select_paged_tokens(

@@ -436,3 +436,51 @@ def test_steps_captured_in_a_cuda_graph(rows):
         assert torch.equal(got[0], idx) and torch.equal(got[1], out)
         assert torch.equal(got[2], idx2) and torch.equal(got[3], out2)
         assert torch.equal(idx, idx2)
+
+
+def test_concurrent_streams_and_host_threads():
+    # two batches (one fused, one chained) on two streams at once, from two
+    # host threads (ctypes releases the GIL, so the library's per-device
+    # caches and launches race for real): each result equals its batch's
+    # result computed alone
+    import threading
+    n = qsa.qsa_select_attend_fused_rows()
+    batches = [W.build("cc_a", [131072, 9215, 519, 40000] * 2, seed=31, device=DEV),
+               W.build("cc_b", [70001, 3, 2052, 131072] * ((n + 4) // 4), seed=32, device=DEV)]
+    assert qsa.qsa_select_attend_fused_cluster(8, batches[0].cmp_page_table.shape[1]) > 0
+    assert batches[1].R > n                                   # the chained kernels
+
+    def run(w, stream):
+        ws = torch.empty(qsa.qsa_select_attend_workspace_bytes(w.R, w.cmp_page_table.shape[1]),
+                         dtype=torch.uint8, device=DEV)
+        res = []
+        for _ in range(10):
+            res.append(qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table,
+                                             w.token_to_request, w.seq_lens, w.query_positions,
+                                             w.q_attn, w.k_view, w.v_view, w.kv_page_table,
+                                             workspace=ws, stream=stream))
+        stream.synchronize()
+        return res
+
+    alone = []
+    for w in batches:
+        s = torch.cuda.Stream()
+        alone.append(run(w, s)[0])
+    out = [None, None]
+    errs = []
+
+    def worker(i):
+        try:
+            out[i] = run(batches[i], torch.cuda.Stream())
+        except Exception as e:          # reported below; a thread cannot fail the test
+            errs.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errs, errs
+    for i in range(2):
+        for idx, o in out[i]:
+            assert torch.equal(idx, alone[i][0]) and torch.equal(o, alone[i][1])
