@@ -33,9 +33,10 @@
  *     error_word is not NULL.  Kernels never trap.
  *   - Concurrent calls that share a workspace race; give each stream its own.
  *   - Any host thread may call.  The work runs on the calling thread's current
- *     device (cudaGetDevice), to which the call binds the thread's CUDA
- *     context before it launches; the stream and every pointer must belong
- *     to that device.
+ *     device (cudaGetDevice): when no context or that device's primary
+ *     context is current, the call binds the thread to the primary context
+ *     before it launches (a context the caller made current itself is used
+ *     as it is); the stream and every pointer must belong to that context.
  *   - FP16 tensors must start on a 16-byte boundary; int tensors on their
  *     element size.  num_rows == 0 is a legal no-op.
  */
