@@ -484,3 +484,42 @@ def test_concurrent_streams_and_host_threads():
     for i in range(2):
         for idx, o in out[i]:
             assert torch.equal(idx, alone[i][0]) and torch.equal(o, alone[i][1])
+
+
+_CAPTURE_FIRST = r"""
+import sys, torch
+import sparse_paged_attention_qsa_gb300 as qsa
+from sparse_paged_attention_qsa_gb300 import workloads as W
+rows = int(sys.argv[1])
+w = W.build("cap", ([131072, 9215, 519, 40000] * rows)[:rows], seed=3, device="cuda")
+R, cols = w.R, w.cmp_page_table.shape[1]
+idx = torch.empty((R, 2051), dtype=torch.int32, device="cuda")
+out = torch.empty((R, 3, 256), dtype=torch.float16, device="cuda")
+ws = torch.empty(qsa.qsa_select_attend_workspace_bytes(R, cols), dtype=torch.uint8, device="cuda")
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):     # the library's first calls in this process
+    qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request, w.seq_lens,
+                          w.query_positions, w.q_attn, w.k_view, w.v_view, w.kv_page_table,
+                          indices=idx, out=out, workspace=ws, stream=s)
+g.replay()
+torch.cuda.synchronize()
+i2, o2 = qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table, w.token_to_request,
+                               w.seq_lens, w.query_positions, w.q_attn, w.k_view, w.v_view,
+                               w.kv_page_table)
+torch.cuda.synchronize()
+sys.exit(0 if torch.equal(i2, idx) and torch.equal(o2, out) else 3)
+"""
+
+
+@pytest.mark.parametrize("rows", [8, 200])
+def test_first_call_inside_a_graph_capture(rows):
+    # a fresh process whose first calls into the library happen while a CUDA
+    # graph is being captured (its one-time setup runs during the capture):
+    # the fused (8 rows) and chained (200 rows) steps replay like eager calls
+    import subprocess
+    import sys
+    root = __file__.rsplit("/tests/", 1)[0]
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST, str(rows)], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
