@@ -37,6 +37,11 @@
  *     context is current, the call binds the thread to the primary context
  *     before it launches (a context the caller made current itself is used
  *     as it is); the stream and every pointer must belong to that context.
+ *     The one-time setup of the large-shared-memory kernels (their attribute
+ *     and occupancy queries) is kept per device for the life of the
+ *     process: after cudaDeviceReset, or from a second context on the same
+ *     device, launches fail with QSA_ERR_CUDA (nothing runs) rather than
+ *     redo it.
  *   - FP16 tensors must start on a 16-byte boundary; int tensors on their
  *     element size.  num_rows == 0 is a legal no-op.
  */
