@@ -191,7 +191,13 @@ def _tag(t: torch.Tensor) -> int:
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
-    return None if t is None else (t.data_ptr() or None)
+    # the library reads and writes device memory only: a host tensor's address
+    # would reach a kernel as an invalid device address
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        raise QSAError(1, f"every tensor must be in CUDA device memory (got a {t.device} tensor)")
+    return t.data_ptr() or None
 
 
 def _stream(stream) -> int | None:

@@ -11,6 +11,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import sparse_paged_attention_qsa_gb300 as qsa
 from sparse_paged_attention_qsa_gb300 import build as qbuild
@@ -394,3 +395,24 @@ def test_fused_cost_fit_constants_agree():
         fused = c["kFusedBaseCost"] + c["kFusedPageCost"] * -(-cols // cs)
         chain = c["kChainBaseCost"] + c["kChainPageCost"] * R * cols
         assert tf._fused_wins(R, cols, cs) == (fused <= chain)
+
+
+def test_binding_rejects_host_tensors(lib):
+    # host (CPU) tensors would reach the kernels as invalid device addresses:
+    # the binding refuses them before calling the library
+    from sparse_paged_attention_qsa_gb300 import workloads as W
+    w = W.config(0, device="cpu")
+    calls = [
+        lambda: qsa.qsa_select_paged_tokens(w.q_sel, w.cmp_cache, w.cmp_page_table,
+                                            w.token_to_request, w.seq_lens, w.query_positions),
+        lambda: qsa.qsa_sparse_attention(w.q_attn, w.k_view, w.v_view, w.kv_page_table,
+                                         w.token_to_request,
+                                         torch.zeros((1, 2051), dtype=torch.int32)),
+        lambda: qsa.qsa_select_attend(w.q_sel, w.cmp_cache, w.cmp_page_table,
+                                      w.token_to_request, w.seq_lens, w.query_positions,
+                                      w.q_attn, w.k_view, w.v_view, w.kv_page_table),
+    ]
+    for call in calls:
+        with pytest.raises(qsa.QSAError) as e:
+            call()
+        assert e.value.status == 1 and "device memory" in str(e.value)
