@@ -200,6 +200,25 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr() or None
 
 
+def _on_current_device(*tensors):
+    """Every tensor given must be in the memory of the current CUDA device,
+    which the library runs on: a host tensor, or one on another GPU, would
+    reach a kernel as an invalid address."""
+    cur = None
+    for t in tensors:
+        if t is None:
+            continue
+        d = t.get_device()                  # -1: host memory
+        if d < 0:
+            raise QSAError(1, f"every tensor must be in CUDA device memory (got a {t.device} "
+                              "tensor)")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if d != cur:
+            raise QSAError(1, f"a tensor is on cuda:{d} but the current device is cuda:{cur} "
+                              "(select it with torch.cuda.device)")
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -231,6 +250,8 @@ def qsa_select_paged_tokens(q_sel, cmp_cache, cmp_page_table, token_to_request, 
     """Selection: returns out [R,2051] int32 (see include/qsa.h).  `library`:
     another loaded build of the C ABI (declare_signatures) instead of libqsa."""
     lib = library or load_library()
+    _on_current_device(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
+                       query_positions, out, workspace, error_word)
     R = q_sel.shape[0] if q_sel.dim() == 3 else -1
     if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
         raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
@@ -268,6 +289,8 @@ def qsa_sparse_attention(q, k_cache, v_cache, kv_page_table, token_to_request, i
     k_cache / v_cache are the exact-packed views (strides [262144,512,256,1],
     V at storage offset 256 of the same buffer)."""
     lib = load_library()
+    _on_current_device(q, k_cache, v_cache, kv_page_table, token_to_request, indices, out,
+                       workspace, error_word)
     if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or indices.dim() != 2:
         raise QSAError(3, "q [R,3,256], k/v [P,512,1,256], indices [R,W] expected")
     if k_cache.shape != v_cache.shape:
@@ -343,6 +366,9 @@ def qsa_select_attend(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_le
     FP16.  Both page tables are indexed by token_to_request.  `library` as in
     qsa_select_paged_tokens."""
     lib = library or load_library()
+    _on_current_device(q_sel, cmp_cache, cmp_page_table, token_to_request, seq_lens,
+                       query_positions, q_attn, k_cache, v_cache, kv_page_table, indices, out,
+                       workspace, error_word)
     if q_sel.dim() != 3 or cmp_cache.dim() != 4 or cmp_page_table.dim() != 2:
         raise QSAError(3, "q_sel must be [R,4,128], cmp_cache [P,128,1,128], page table 2-D")
     if q_attn.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or kv_page_table.dim() != 2:
@@ -401,6 +427,8 @@ def qsa_build_metadata(query_start_loc, seq_lens, block_table, num_tokens: int, 
     is not given it is read from the device (one synchronising read).
     ``out`` may hold preallocated tensors under the same keys."""
     lib = load_library()
+    _on_current_device(query_start_loc, seq_lens, block_table, common_slot_mapping,
+                       *(out or {}).values())
     dev = query_start_loc.device
     num_reqs = query_start_loc.numel() - 1
     if query_start_loc.dim() != 1 or seq_lens.dim() != 1 or block_table.dim() != 2:
@@ -448,6 +476,7 @@ def qsa_paged_mqa_logits(q, kv_cache, weights, context_lens, block_tables, next_
     [num_blocks, block_size*132] bytes (uint8 or float8_e4m3fn storage).
     `library` as in qsa_select_paged_tokens."""
     lib = library or load_library()
+    _on_current_device(q, kv_cache, weights, context_lens, block_tables, out, error_word)
     if q.dim() != 3 or kv_cache.dim() != 2 or weights.dim() != 2 or block_tables.dim() != 2:
         raise QSAError(3, "q [rows,H,128], kv_cache [blocks, bs*132], weights [rows,H], "
                           "block_tables 2-D expected")
@@ -482,6 +511,7 @@ def qsa_top_k_per_row_decode(logits, next_n: int, seq_lens, topk_tokens: int, ou
     """Per-row top-k of the indexer logits (include/qsa_indexer.h): returns
     int32 [rows, topk_tokens], -1 padded."""
     lib = load_library()
+    _on_current_device(logits, seq_lens, out)
     if logits.dim() != 2:
         raise QSAError(3, "logits must be 2-D")
     rows, cols = logits.shape
