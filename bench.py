@@ -483,9 +483,23 @@ def run_ours(args, world, rank, local):
         rate, dt = oracle_rate(sample, n, threads)
         n1 = max(2, int(rate / threads * 3.0))                           # about 3 s on one core
         rate1, _ = oracle_rate(sample, n1, 1)
+        # the GPU step timed again after the CPU leg (GPU, CPU, GPU): its
+        # drift from the first timing, in percent
+        Kd = max(1, min(K, 100))
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        d0.record(stream)
+        for _ in range(Kd):
+            select()
+            attend()
+        d1.record(stream)
+        torch.cuda.synchronize(dev)
+        drift = (d0.elapsed_time(d1) / Kd / (total_ms / K) - 1.0) * 100.0
         cpu = {"value": rate, "unit": "rows/s", "cores": threads, "threads": threads,
                "host_cores": total_cores, "kind": "oracle",
                "single_thread_value": rate1,
+               "gpu_step_drift_pct": drift,
                "sample": f"{n} decode rows (select+attend) over {len(sample.rows)} rows of "
                          f"this workload, plain C oracle on {threads} threads, {dt:.1f} s wall"}
 
